@@ -1,0 +1,115 @@
+"""Seeded synthetic inputs for block-diffusion attention workloads.
+
+This module holds workload shapes and random number generation only: no step
+of the attention method.  Both the CUDA path's tests/benchmark and the CPU
+oracle's checks draw their inputs from here.
+
+Every tensor is drawn as float32 N(0, 1) from one torch generator seeded with
+`seed`, in the fixed order q_clean, k_clean, v_clean, q_corr, k_corr, v_corr,
+do_clean, do_corr, then rounded to bfloat16 (round-to-nearest-even).  The
+long fine-tune workload scales K of each KV head by s ~ U(0.5, 2) (drawn after
+the tensors, before the bf16 rounding) to vary softmax sharpness.  Layout of
+every tensor: [batch, L, heads, d] contiguous.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    L: int          # clean length = corrupted length
+    M: int          # block size
+    Hq: int
+    Hkv: int
+    d: int
+    P: int = 1      # virtual clean shards (1 = unsharded fused path)
+    has_clean_queries: bool = True
+    k_scale_range: tuple | None = None   # per-KV-head K scale ~ U(lo, hi)
+    seed: int = 1234
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def B(self) -> int:
+        return self.L // self.M
+
+    def pairs_per_head(self) -> int:
+        """Allowed (query, key) pairs per query head: L(L+M) with clean
+        queries, L(L+M)/2 with corrupted queries only."""
+        full = self.L * (self.L + self.M)
+        return full if self.has_clean_queries else full // 2
+
+    def useful_fwd_flops(self) -> float:
+        """QK^T and PV over allowed pairs: 4 d flops per pair per query head."""
+        return 4.0 * self.d * self.pairs_per_head() * self.Hq * self.batch
+
+    def useful_bwd_flops(self) -> float:
+        """Backward at 2.5x forward (S recompute, dP, dV, dK, dQ)."""
+        return 2.5 * self.useful_fwd_flops()
+
+
+WORKLOADS = {
+    # tiny MHA case the oracle finishes in seconds
+    "tiny": Workload("tiny", 1, 1024, 64, 2, 2, 64, seed=1234),
+    # dense 14B-like layer, GQA 40/8
+    "dense14b": Workload("dense14b", 1, 16384, 32, 40, 8, 128, seed=1235),
+    # context-sharded: P=8 virtual clean shards of 8192 tokens
+    "sharded": Workload("sharded", 1, 65536, 64, 32, 8, 128, P=8, seed=1236),
+    # long fine-tune layer, per-KV-head K scale, P=16
+    "long": Workload("long", 1, 131072, 32, 32, 4, 128, P=16,
+                     k_scale_range=(0.5, 2.0), seed=1237),
+    # drafter: corrupted queries only over a 1M clean context
+    "drafter": Workload("drafter", 1, 1048576, 16, 32, 8, 128,
+                        has_clean_queries=False, seed=1238),
+}
+
+
+def make_inputs(w: Workload, device="cuda", seed: int | None = None,
+                L: int | None = None) -> dict:
+    """Draw the workload's tensors on `device` (bf16, [batch, L, H, d]).
+
+    `L` overrides the sequence length (same recipe, for scaled-down cases).
+    """
+    L = w.L if L is None else L
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed if seed is None else seed)
+
+    def draw(h):
+        return torch.randn((w.batch, L, h, w.d), generator=g, device=device,
+                           dtype=torch.float32)
+
+    out = {}
+    raw = {}
+    for name, h in (("q_clean", w.Hq), ("k_clean", w.Hkv), ("v_clean", w.Hkv),
+                    ("q_corr", w.Hq), ("k_corr", w.Hkv), ("v_corr", w.Hkv),
+                    ("do_clean", w.Hq), ("do_corr", w.Hq)):
+        if not w.has_clean_queries and name in ("q_clean", "do_clean"):
+            continue
+        raw[name] = draw(h)
+    if w.k_scale_range is not None:
+        lo, hi = w.k_scale_range
+        s = lo + (hi - lo) * torch.rand((w.Hkv,), generator=g, device=device,
+                                        dtype=torch.float32)
+        raw["k_clean"] = raw["k_clean"] * s.view(1, 1, -1, 1)
+        raw["k_corr"] = raw["k_corr"] * s.view(1, 1, -1, 1)
+    for name, t in raw.items():
+        out[name] = t.to(torch.bfloat16)
+    if not w.has_clean_queries:
+        out["q_clean"] = None
+        out["do_clean"] = None
+    return out
+
+
+def to_f64(t):
+    """bf16 torch tensor (any device) -> float64 numpy array (exact up-cast)."""
+    if t is None:
+        return None
+    return t.detach().to("cpu").to(torch.float64).numpy()

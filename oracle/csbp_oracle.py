@@ -1,0 +1,524 @@
+"""Float64 CPU oracle for two-copy block-diffusion attention (CSBP per-rank math).
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute this module; only the test suite, the smoke check and the CPU-baseline
+leg of the benchmark use it.  It shares no code with the CUDA library.
+
+Every function is the plain definition written out in float64 NumPy, in the
+order and notation of the pages it follows:
+
+* [Blog] "CSBP 完全拆解：块并行如何让长上下文扩散语言模型少传无效 KV"
+  (pinghaoyang.com.cn), sections
+    - "块扩散模型到底多了哪一种并行机会"  (block partition x = (x^(1)..x^(B)),
+      M = L/B, factorisation p(x) = prod_b p(x^(b) | x^(<b)))
+    - "传统上下文并行为什么会传错东西"  (O_r = softmax(Q_r K^T / sqrt(d_h) + M_r) V;
+      a corrupted query of block b needs exactly [K_b; K^clean_<b], [V_b; V^clean_<b])
+    - "BP：把损坏块留在本地"  (L_r = sum_{b in B_r} L_b, sum_r grad L_r = grad L)
+    - "CSBP：BP 管损坏块，CP 管干净上下文"  (O_b = Attn(Q_b, [K_b; K^clean_<b],
+      [V_b; V^clean_<b]); corrupted grads stay local, clean dK/dV go to the
+      clean-shard owner)
+    - "在线 softmax 合并：为什么分两段算仍是同一个注意力"  (m = max(z1, z2),
+      w_i = e^(z_i - m), O = (w1 O1 + w2 O2)/(w1 + w2), z = m + log(w1 + w2))
+    - "负载均衡：为什么要首尾块配对"  (block b paired with block B+1-b;
+      zigzag pairing of early and late clean chunks)
+* [Project] "Block Parallelism for Efficient Distributed Long-Context Diffusion
+  Language Model Training" (Turbo-dLLM project page), sections "Method"
+  (corrupted K/V are read only by their own block) and "Load balancing:
+  pairing early and late blocks" (block b and block B+1-b share a rank; the
+  same early-late pairing shards the clean sequence; every pair does
+  identical work).
+* [Wiki] "CSBP: stop sharding by token position, start sharding by what the
+  loss actually needs", "TL;DR" (a length-L example runs as 2L positions: a
+  clean copy and a corrupted copy).
+
+Readings taken where the pages are silent (each is also listed in the design
+notes): clean queries attend block-causally over the clean copy (b_j <= b_i);
+clean queries never read corrupted keys; GQA maps query head h to KV head
+h // (Hq / Hkv); the LSE is the natural log of the softmax denominator; blocks
+map to shards through 2P contiguous clean chunks, shard r owning chunks r and
+2P-1-r; a sharded forward takes one partial per clean shard plus one "own"
+(corrupted own-block) partial for every query row.
+
+Positions are 0-based inside each copy; block id blk(i) = i // M.
+Stream 0 = clean copy, stream 1 = corrupted copy.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+CLEAN = 0
+CORR = 1
+
+
+# --------------------------------------------------------------------------
+# Mask  ([Blog] "传统上下文并行为什么会传错东西" and "CSBP：BP 管损坏块，CP 管干净上下文";
+#        [Project] "Method")
+# --------------------------------------------------------------------------
+def allowed(q_stream: int, i: int, k_stream: int, j: int, M: int) -> bool:
+    """Scalar mask predicate: may query (q_stream, i) read key (k_stream, j)?
+
+    corrupted q -> corrupted k : same block (bidirectional inside the block)
+    corrupted q -> clean k     : strictly earlier block  (K^clean_<b)
+    clean q     -> clean k     : same or earlier block   (block-causal reading)
+    clean q     -> corrupted k : never (corrupted K/V are read by their own
+                                 block only)
+    """
+    bi, bj = i // M, j // M
+    if q_stream == CORR and k_stream == CORR:
+        return bj == bi
+    if q_stream == CORR and k_stream == CLEAN:
+        return bj < bi
+    if q_stream == CLEAN and k_stream == CLEAN:
+        return bj <= bi
+    return False
+
+
+def bd_mask(L: int, M: int) -> np.ndarray:
+    """Explicit boolean mask A[2L, 2L] over (query, key) positions.
+
+    Rows/cols 0..L-1 are the clean copy, L..2L-1 the corrupted copy.  Built
+    from the block ids by broadcasting the four cases of `allowed`.
+    """
+    if L % M != 0:
+        raise ValueError("L must be a multiple of the block size M")
+    b = np.arange(L) // M
+    bq, bk = b[:, None], b[None, :]
+    A = np.zeros((2 * L, 2 * L), dtype=bool)
+    A[:L, :L] = bk <= bq          # clean q, clean k
+    A[:L, L:] = False             # clean q, corrupted k
+    A[L:, :L] = bk < bq           # corrupted q, clean k
+    A[L:, L:] = bk == bq          # corrupted q, corrupted k
+    return A
+
+
+def mask_row(q_stream: int, i: int, L: int, M: int) -> np.ndarray:
+    """Row (q_stream, i) of `bd_mask`, length 2L (clean keys then corrupted)."""
+    b = np.arange(L) // M
+    bi = i // M
+    row = np.zeros(2 * L, dtype=bool)
+    if q_stream == CLEAN:
+        row[:L] = b <= bi
+    else:
+        row[:L] = b < bi
+        row[L:] = b == bi
+    return row
+
+
+# --------------------------------------------------------------------------
+# Scaled softmax attention over an explicit mask
+# ([Blog] "传统上下文并行为什么会传错东西": O = softmax(Q K^T / sqrt(d_h) + M) V)
+# --------------------------------------------------------------------------
+def masked_attention(q, k, v, allow, scale):
+    """q [Nq,d], k/v [Nk,d], allow [Nq,Nk] bool -> (O [Nq,d], lse [Nq]).
+
+    Rows with no allowed key get O = 0 and lse = -inf (an empty part of a
+    partition; used by the sharded forward).
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    s = scale * (q @ k.T)
+    s = np.where(allow, s, -np.inf)
+    m = s.max(axis=1)
+    empty = ~np.isfinite(m)
+    m_safe = np.where(empty, 0.0, m)
+    p = np.exp(s - m_safe[:, None])            # exp(-inf) = 0 off the mask
+    l = p.sum(axis=1)
+    l_safe = np.where(empty, 1.0, l)
+    o = (p @ v) / l_safe[:, None]
+    o[empty] = 0.0
+    lse = np.where(empty, -np.inf, m_safe + np.log(l_safe))
+    return o, lse
+
+
+def masked_attention_bwd(q, k, v, allow, scale, do):
+    """Analytic VJP of `masked_attention` for upstream gradient dO.
+
+    P = softmax(S), dV = P^T dO, dP = dO V^T, D_i = sum_j P_ij dP_ij,
+    dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+    Returns (dQ, dK, dV, D).
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.asarray(do, np.float64)
+    s = scale * (q @ k.T)
+    s = np.where(allow, s, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    m = np.where(np.isfinite(m), m, 0.0)
+    e = np.exp(s - m)
+    l = e.sum(axis=1, keepdims=True)
+    p = e / np.where(l > 0, l, 1.0)
+    dv = p.T @ do
+    dp = do @ v.T
+    D = (p * dp).sum(axis=1)
+    ds = p * (dp - D[:, None])
+    dq = scale * (ds @ k)
+    dk = scale * (ds.T @ q)
+    return dq, dk, dv, D
+
+
+# --------------------------------------------------------------------------
+# Two-copy block-diffusion attention, multi-head with GQA
+# --------------------------------------------------------------------------
+def _stack_streams(x_clean, x_corr):
+    """[L,H,d] clean and corrupted -> [2L,H,d] (clean first)."""
+    return np.concatenate([np.asarray(x_clean, np.float64),
+                           np.asarray(x_corr, np.float64)], axis=0)
+
+
+def bd_attention_fwd(qc, kc, vc, qx, kx, vx, M, scale):
+    """Full forward of two-copy block-diffusion attention.
+
+    Inputs [L, H, d] (H = Hq for q, Hkv for k/v); qc may be None for the
+    corrupted-queries-only (drafter) workload.  Returns
+    (Oc [L,Hq,d] or None, Ox [L,Hq,d], lse [2,Hq,L] with NaN rows for an absent
+    clean query stream).
+    """
+    L, Hkv, d = np.shape(kc)
+    Hq = np.shape(qx)[1]
+    G = Hq // Hkv
+    A = bd_mask(L, M)
+    K = _stack_streams(kc, kx)
+    V = _stack_streams(vc, vx)
+    has_clean = qc is not None
+    Oc = np.zeros((L, Hq, d)) if has_clean else None
+    Ox = np.zeros((L, Hq, d))
+    lse = np.full((2, Hq, L), np.nan)
+    for h in range(Hq):
+        g = h // G
+        if has_clean:
+            o, z = masked_attention(np.asarray(qc, np.float64)[:, h], K[:, g], V[:, g],
+                                    A[:L], scale)
+            Oc[:, h], lse[0, h] = o, z
+        o, z = masked_attention(np.asarray(qx, np.float64)[:, h], K[:, g], V[:, g],
+                                A[L:], scale)
+        Ox[:, h], lse[1, h] = o, z
+    return Oc, Ox, lse
+
+
+def bd_attention_bwd(qc, kc, vc, qx, kx, vx, doc, dox, M, scale):
+    """Analytic backward of `bd_attention_fwd`.
+
+    Returns dict with dq_clean, dq_corr, dk_clean, dv_clean, dk_corr, dv_corr
+    (dK/dV summed over the G query heads of each KV head) and D [2,Hq,L].
+    Clean dK/dV collect contributions from clean queries (same or later block)
+    and corrupted queries (later blocks); corrupted dK/dV only from queries of
+    their own block ([Blog] "CSBP：BP 管损坏块，CP 管干净上下文", backward paragraph).
+    """
+    L, Hkv, d = np.shape(kc)
+    Hq = np.shape(qx)[1]
+    G = Hq // Hkv
+    A = bd_mask(L, M)
+    K = _stack_streams(kc, kx)
+    V = _stack_streams(vc, vx)
+    has_clean = qc is not None
+    if has_clean:
+        Q = _stack_streams(qc, qx)
+        dO = _stack_streams(doc, dox)
+        rows = slice(0, 2 * L)
+    else:
+        Q = np.concatenate([np.zeros((L, Hq, d)), np.asarray(qx, np.float64)], 0)
+        dO = np.concatenate([np.zeros((L, Hq, d)), np.asarray(dox, np.float64)], 0)
+        rows = slice(L, 2 * L)
+    dQ = np.zeros((2 * L, Hq, d))
+    dK = np.zeros((2 * L, Hkv, d))
+    dV = np.zeros((2 * L, Hkv, d))
+    D = np.full((2, Hq, L), np.nan)
+    for h in range(Hq):
+        g = h // G
+        dq, dk, dv, Dh = masked_attention_bwd(Q[rows, h], K[:, g], V[:, g], A[rows],
+                                              scale, dO[rows, h])
+        dQ[rows, h] = dq
+        dK[:, g] += dk
+        dV[:, g] += dv
+        if has_clean:
+            D[0, h], D[1, h] = Dh[:L], Dh[L:]
+        else:
+            D[1, h] = Dh
+    return {
+        "dq_clean": dQ[:L] if has_clean else None, "dq_corr": dQ[L:],
+        "dk_clean": dK[:L], "dv_clean": dV[:L],
+        "dk_corr": dK[L:], "dv_corr": dV[L:], "D": D,
+    }
+
+
+# --------------------------------------------------------------------------
+# Log-sum-exp merge  ([Blog] "在线 softmax 合并：为什么分两段算仍是同一个注意力")
+# --------------------------------------------------------------------------
+def lse_merge_pair(o1, z1, o2, z2):
+    """Merge two normalised partial outputs over disjoint key sets.
+
+    m = max(z1, z2); w_i = exp(z_i - m); O = (w1 O1 + w2 O2) / (w1 + w2);
+    z = m + log(w1 + w2).  A part with z = -inf has w = 0 (it read no key).
+    o* [rows, ...], z* [rows].
+    """
+    z1 = np.asarray(z1, np.float64)
+    z2 = np.asarray(z2, np.float64)
+    m = np.maximum(z1, z2)
+    both_empty = ~np.isfinite(m)
+    m_safe = np.where(both_empty, 0.0, m)
+    w1 = np.exp(z1 - m_safe)
+    w2 = np.exp(z2 - m_safe)
+    wsum = w1 + w2
+    wsum_safe = np.where(both_empty, 1.0, wsum)
+    shape = (-1,) + (1,) * (np.ndim(o1) - 1)
+    o = (w1.reshape(shape) * o1 + w2.reshape(shape) * o2) / wsum_safe.reshape(shape)
+    o = np.where(both_empty.reshape(shape), 0.0, o)
+    z = np.where(both_empty, -np.inf, m_safe + np.log(wsum_safe))
+    return o, z
+
+
+def lse_merge(o_parts, z_parts):
+    """Merge n partials by applying the two-part merge left to right."""
+    o, z = np.asarray(o_parts[0], np.float64), np.asarray(z_parts[0], np.float64)
+    for s in range(1, len(o_parts)):
+        o, z = lse_merge_pair(o, z, np.asarray(o_parts[s], np.float64), z_parts[s])
+    return o, z
+
+
+# --------------------------------------------------------------------------
+# Block / clean-chunk ownership: dual-end pairing and zigzag clean sharding
+# ([Blog] "负载均衡：为什么要首尾块配对"; [Project] "Load balancing: pairing early
+#  and late blocks")
+# --------------------------------------------------------------------------
+def chunk_owner(L: int, P: int) -> np.ndarray:
+    """Owner shard of each of the 2P contiguous clean chunks (length L/(2P)).
+
+    Shard r owns chunk r and chunk 2P-1-r: the early/late (zigzag) pairing.
+    """
+    if L % (2 * P) != 0:
+        raise ValueError("L must be a multiple of 2P")
+    owner = np.empty(2 * P, dtype=np.int32)
+    for r in range(P):
+        owner[r] = r
+        owner[2 * P - 1 - r] = r
+    return owner
+
+
+def block_owner(L: int, M: int, P: int) -> np.ndarray:
+    """Owner shard of each corrupted block: the owner of the clean chunk that
+    holds the block's first position.  With B % 2P == 0 this pairs block b
+    with block B-1-b (0-based), i.e. the pages' b with B+1-b (1-based)."""
+    B = L // M
+    if L % M != 0 or B % (2 * P) != 0:
+        raise ValueError("need L % M == 0 and B % 2P == 0")
+    cl = L // (2 * P)
+    co = chunk_owner(L, P)
+    return np.array([co[(b * M) // cl] for b in range(B)], dtype=np.int32)
+
+
+def pair_counts_per_owner(L, M, P, owner_of_block, has_clean_queries=True):
+    """Allowed (query, key) pairs charged to each owner when owner r computes
+    every query row of the blocks it owns (both copies), over all keys."""
+    B = L // M
+    counts = np.zeros(P, dtype=np.int64)
+    for b in range(B):
+        r = owner_of_block[b]
+        # corrupted queries of block b: M own + b*M clean keys each
+        counts[r] += M * (M + b * M)
+        if has_clean_queries:
+            # clean queries of block b: (b+1)*M clean keys each
+            counts[r] += M * ((b + 1) * M)
+    return counts
+
+
+def pair_counts_from_mask(L, M, P, owner_of_block, has_clean_queries=True):
+    """Brute-force version of `pair_counts_per_owner` from the explicit mask."""
+    A = bd_mask(L, M)
+    counts = np.zeros(P, dtype=np.int64)
+    per_row = A.sum(axis=1)
+    for i in range(L):
+        r = owner_of_block[i // M]
+        if has_clean_queries:
+            counts[r] += per_row[i]
+        counts[r] += per_row[L + i]
+    return counts
+
+
+# --------------------------------------------------------------------------
+# Sharded forward: per-part partial attention merged by LSE
+# ([Blog] "在线 softmax 合并" implementation schedule steps 2-4, generalised to
+#  one partial per clean shard plus the corrupted own-block part)
+# --------------------------------------------------------------------------
+def key_parts(L: int, P: int) -> np.ndarray:
+    """Part id of each of the 2L keys: clean key j -> owner of its chunk,
+    corrupted key -> part P ("own")."""
+    co = chunk_owner(L, P)
+    cl = L // (2 * P)
+    part = np.empty(2 * L, dtype=np.int32)
+    part[:L] = co[np.arange(L) // cl]
+    part[L:] = P
+    return part
+
+
+def bd_attention_fwd_sharded(qc, kc, vc, qx, kx, vx, M, scale, P):
+    """Forward via P+1 partials per query row and the LSE merge.
+
+    Returns (Oc, Ox, lse, partials) where partials = (o_parts [P+1,2,L,Hq,d],
+    z_parts [P+1,2,Hq,L]); a part that holds no allowed key of a row has
+    z = -inf and O = 0.
+    """
+    L, Hkv, d = np.shape(kc)
+    Hq = np.shape(qx)[1]
+    G = Hq // Hkv
+    A = bd_mask(L, M)
+    K = _stack_streams(kc, kx)
+    V = _stack_streams(vc, vx)
+    part = key_parts(L, P)
+    has_clean = qc is not None
+    o_parts = np.zeros((P + 1, 2, L, Hq, d))
+    z_parts = np.full((P + 1, 2, Hq, L), -np.inf)
+    streams = [(CLEAN, qc), (CORR, qx)] if has_clean else [(CORR, qx)]
+    for s in range(P + 1):
+        in_part = part == s
+        for st, q in streams:
+            rows = A[:L] if st == CLEAN else A[L:]
+            for h in range(Hq):
+                g = h // G
+                o, z = masked_attention(np.asarray(q, np.float64)[:, h], K[:, g], V[:, g],
+                                        rows & in_part[None, :], scale)
+                o_parts[s, st, :, h] = o
+                z_parts[s, st, h] = z
+    Oc = np.zeros((L, Hq, d)) if has_clean else None
+    Ox = np.zeros((L, Hq, d))
+    lse = np.full((2, Hq, L), np.nan)
+    for st in ([CLEAN, CORR] if has_clean else [CORR]):
+        for h in range(Hq):
+            o, z = lse_merge([o_parts[s, st, :, h] for s in range(P + 1)],
+                             [z_parts[s, st, h] for s in range(P + 1)])
+            if st == CLEAN:
+                Oc[:, h] = o
+            else:
+                Ox[:, h] = o
+            lse[st, h] = z
+    return Oc, Ox, lse, (o_parts, z_parts)
+
+
+# --------------------------------------------------------------------------
+# Tile schedule derived from the mask
+# --------------------------------------------------------------------------
+def tile_pairs(L, M, Tq, Tkv, P=1, has_clean_queries=True):
+    """Set of (q_stream, q_tile, kv_stream, kv_tile, full, part) over every
+    (query-tile, key-tile) pair holding at least one allowed entry.
+
+    full = every entry of the tile is allowed.  part = owner shard of the
+    clean chunk holding the key tile (clean keys) or P (corrupted keys).
+    Requires Tkv to divide L/(2P) so a key tile lies in one chunk.
+    """
+    if (L // (2 * P)) % Tkv != 0 and P > 1:
+        raise ValueError("Tkv must divide L/(2P)")
+    A = bd_mask(L, M)
+    if P == 1:
+        part = np.concatenate([np.zeros(L, np.int32), np.ones(L, np.int32)])
+    else:
+        part = key_parts(L, P)
+    nq = -(-L // Tq)
+    nk = -(-L // Tkv)
+    out = set()
+    qstreams = [CLEAN, CORR] if has_clean_queries else [CORR]
+    for qs in qstreams:
+        for qt in range(nq):
+            r0, r1 = qs * L + qt * Tq, qs * L + min((qt + 1) * Tq, L)
+            for ks in (CLEAN, CORR):
+                for kt in range(nk):
+                    c0, c1 = ks * L + kt * Tkv, ks * L + min((kt + 1) * Tkv, L)
+                    blk = A[r0:r1, c0:c1]
+                    if blk.any():
+                        out.add((qs, qt, ks, kt, bool(blk.all()), int(part[c0])))
+    return out
+
+
+# --------------------------------------------------------------------------
+# Row / key sampled evaluation for long sequences
+# --------------------------------------------------------------------------
+def sampled_rows(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples):
+    """Exact O, lse, D and dQ for sampled query rows.
+
+    samples: iterable of (q_stream, i, h).  Each row depends only on itself,
+    the full K/V of its KV head and dO_i.  Returns dict keyed by the sample
+    tuple -> (o [d], lse, D, dq [d]).
+    """
+    L, Hkv, d = np.shape(kc)
+    Hq = np.shape(qx)[1]
+    G = Hq // Hkv
+    out = {}
+    kcache = {}
+    for (qs, i, h) in samples:
+        g = h // G
+        if g not in kcache:
+            kcache[g] = (np.concatenate([np.asarray(kc[:, g], np.float64),
+                                         np.asarray(kx[:, g], np.float64)], 0),
+                         np.concatenate([np.asarray(vc[:, g], np.float64),
+                                         np.asarray(vx[:, g], np.float64)], 0))
+        K, V = kcache[g]
+        row = mask_row(qs, i, L, M)
+        q = np.asarray((qc if qs == CLEAN else qx)[i, h], np.float64)[None, :]
+        do = np.asarray((doc if qs == CLEAN else dox)[i, h], np.float64)[None, :]
+        Ks, Vs = K[row], V[row]
+        o, z = masked_attention(q, Ks, Vs, np.ones((1, Ks.shape[0]), bool), scale)
+        dq, _, _, D = masked_attention_bwd(q, Ks, Vs, np.ones((1, Ks.shape[0]), bool),
+                                           scale, do)
+        out[(qs, i, h)] = (o[0], float(z[0]), float(D[0]), dq[0])
+    return out
+
+
+def readers_of_key(k_stream, j, L, M, has_clean_queries=True):
+    """All query rows (q_stream, i) whose mask row allows key (k_stream, j)."""
+    bj = j // M
+    out = []
+    if k_stream == CORR:
+        out += [(CORR, i) for i in range(bj * M, (bj + 1) * M)]
+    else:
+        if has_clean_queries:
+            out += [(CLEAN, i) for i in range(bj * M, L)]
+        out += [(CORR, i) for i in range((bj + 1) * M, L)]
+    return out
+
+
+def sampled_keys(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples):
+    """Exact dK, dV for sampled keys (k_stream, j, g): sums over every reader
+    row of the G query heads of KV head g, each reader's P_ij and dS_ij taken
+    from that row's own full softmax."""
+    L, Hkv, d = np.shape(kc)
+    Hq = np.shape(qx)[1]
+    G = Hq // Hkv
+    has_clean = qc is not None
+    out = {}
+    for (ks, j, g) in samples:
+        K = np.concatenate([np.asarray(kc[:, g], np.float64), np.asarray(kx[:, g], np.float64)], 0)
+        V = np.concatenate([np.asarray(vc[:, g], np.float64), np.asarray(vx[:, g], np.float64)], 0)
+        col = ks * L + j
+        dk = np.zeros(d)
+        dv = np.zeros(d)
+        for (qs, i) in readers_of_key(ks, j, L, M, has_clean):
+            row = mask_row(qs, i, L, M)
+            for h in range(g * G, (g + 1) * G):
+                q = np.asarray((qc if qs == CLEAN else qx)[i, h], np.float64)[None, :]
+                do = np.asarray((doc if qs == CLEAN else dox)[i, h], np.float64)[None, :]
+                s = scale * (q @ K[row].T)[0]
+                m = s.max()
+                e = np.exp(s - m)
+                p_row = e / e.sum()
+                dp_row = (do @ V[row].T)[0]
+                D = float((p_row * dp_row).sum())
+                idx = int(np.flatnonzero(np.flatnonzero(row) == col)[0])
+                p = p_row[idx]
+                ds = p * (dp_row[idx] - D)
+                dv += p * do[0]
+                dk += scale * ds * q[0]
+        out[(ks, j, g)] = (dk, dv)
+    return out
+
+
+# --------------------------------------------------------------------------
+# Useful (mask-allowed) work
+# ([Blog] "CSBP：BP 管损坏块，CP 管干净上下文": CP and CSBP compute the same legal
+#  pairs, Theta(L^2) in total)
+# --------------------------------------------------------------------------
+def allowed_pairs_per_head(L, M, has_clean_queries=True):
+    """Number of allowed (query, key) pairs for one query head."""
+    B = L // M
+    corr = sum(M * (M + b * M) for b in range(B))
+    clean = sum(M * ((b + 1) * M) for b in range(B)) if has_clean_queries else 0
+    return corr + clean
