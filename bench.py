@@ -1,0 +1,340 @@
+"""Benchmark: fused two-copy block-diffusion attention, forward + backward.
+
+One step = one forward and one backward pass over one batch of seeded
+synthetic bf16 inputs, through the C-ABI library (csbp_attn_fwd then
+csbp_attn_bwd; for sharded workloads the forward runs per-shard partials plus
+the LSE merge).  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                  [--impl {csbp,reference}] [--no-cpu-baseline]
+
+metric = useful (mask-allowed) TFLOP/s of fwd+bwd: 4*d FLOPs per allowed
+(query, key) pair per query head forward, 2.5x that backward.  `value` is
+timed with CUDA events on the launch stream with inputs resident in HBM;
+`e2e` repeats the step through the same API with host-pinned inputs copied in
+and the outputs/gradients copied back inside the timed region.
+With N > 1 (torchrun) every rank runs an independent replica of the
+workload on its own GPU (no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "useful TFLOP/s fwd+bwd block-diffusion attention (1 GB300) and % of BF16 peak"
+DEFAULT_CONFIG = "dense14b"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="csbp", choices=["csbp", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16": p.get("bf16_tflops", 1914.7),
+                "bf16_sustained": p.get("bf16_tflops_sustained", 1693.2),
+                "hbm": p.get("hbm_gbs", 6783.8), "source": "measured"}
+    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(",") for ln in self.file if ln.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ cpu oracle
+def cpu_oracle_sample(w, seconds, seed=7):
+    """Time the float64 oracle on seeded sampled query rows of the workload
+    (forward + analytic backward of each row against its full masked key
+    set) until about `seconds` of CPU work; returns useful TFLOP/s and a
+    description.  Inputs are drawn on the CPU with the workload's recipe at a
+    length capped so the sample stays bounded."""
+    import numpy as np
+    import torch
+
+    from block_diffusion_lm_gb300.inputs import make_inputs
+    from oracle import csbp_oracle as O
+
+    L = w.L
+    t = make_inputs(w, "cpu", seed=seed)
+    f = {k: (v[0] if v is not None else None) for k, v in t.items()}
+
+    class View:
+        def __init__(self, x):
+            self.x, self.shape = x, tuple(x.shape)
+
+        def __getitem__(self, idx):
+            return self.x[idx].to(torch.float32).numpy()
+
+    fv = {k: (View(v) if v is not None else None) for k, v in f.items()}
+    rng = np.random.default_rng(seed)
+    streams = [0, 1] if w.has_clean_queries else [1]
+    G = w.Hq // w.Hkv
+    rows_done = 0
+    useful = 0.0
+    t0 = time.perf_counter()
+    batch_rows = 16
+    while time.perf_counter() - t0 < seconds:
+        h = int(rng.integers(0, w.Hq))
+        samples = [(int(rng.choice(streams)), int(rng.integers(0, L)), h) for _ in range(batch_rows)]
+        O.sampled_rows(fv["q_clean"], fv["k_clean"], fv["v_clean"], fv["q_corr"], fv["k_corr"],
+                       fv["v_corr"], fv["do_clean"], fv["do_corr"], w.M, w.scale, samples)
+        for qs, i, _ in samples:
+            b = i // w.M
+            n_allowed = (b + 1) * w.M  # both copies: M(b+1) visible keys
+            useful += 4.0 * w.d * n_allowed * 3.5
+        rows_done += batch_rows
+    dt = time.perf_counter() - t0
+    del G
+    return {"value": useful / dt / 1e12, "unit": "TFLOP/s",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{rows_done} seeded query rows (fwd + analytic bwd per row against all "
+                      f"2L={2 * L} keys, masked), {dt:.1f} s; useful FLOPs counted as in the metric"}
+
+
+# --------------------------------------------------------------- launches
+def launches_per_step(w):
+    """Kernels this library launches per fwd+bwd step (mirrors csbp_api.cu)."""
+    n_qs = 2 if w.has_clean_queries else 1
+    fwd = 1 + ((1 + n_qs * w.batch) if w.P > 1 else 0)   # [fill] + fwd + [merges]
+    bwd = n_qs + 1 + n_qs                                  # pre per stream + main + convert
+    return fwd + bwd
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from block_diffusion_lm_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.config]
+    flops = w.useful_fwd_flops() + w.useful_bwd_flops()
+    config = {"workload": w.name, "batch": w.batch, "L": w.L, "M": w.M, "Hq": w.Hq,
+              "Hkv": w.Hkv, "d": w.d, "P": w.P, "clean_queries": w.has_clean_queries,
+              "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = []
+        for _ in range(args.warmup):
+            cpu_oracle_sample(w, 2.0)
+        for _ in range(args.steps):
+            steps.append(cpu_oracle_sample(w, max(2.0, args.cpu_seconds / max(args.steps, 1))))
+        v = statistics.median(s["value"] for s in steps)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+                "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": flops / (v * 1e12) * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config,
+                "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": steps[0]["cores"],
+                                 "kind": "oracle", "sample": steps[0]["sample"]},
+                "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from block_diffusion_lm_gb300 import build, csbp
+    from block_diffusion_lm_gb300.inputs import make_inputs
+
+    build.build()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+
+    t = make_inputs(w, dev)
+    attn = csbp.BlockDiffusionAttention(w.batch, w.L, w.M, w.Hq, w.Hkv, w.d, P=w.P,
+                                        has_clean_queries=w.has_clean_queries, device=dev)
+    out = attn.alloc_outputs()
+    grads = attn.alloc_grads()
+    in_bytes = sum(v.numel() * v.element_size() for v in t.values() if v is not None)
+
+    def step():
+        attn.forward(t, out=out, stream=stream)
+        attn.backward(t, out, grads=grads, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    attn.check(stream)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    start_all = torch.cuda.Event(enable_timing=True)
+    end_all = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start_all.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            attn.forward(t, out=out, stream=stream)
+            ev[i][1].record(stream)
+            attn.backward(t, out, grads=grads, stream=stream)
+            ev[i][2].record(stream)
+        end_all.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    attn.check(stream)
+    total_ms = start_all.elapsed_time(end_all)
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    if world > 1:
+        x = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        total_ms = x.item()
+        dist.barrier()
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---------------- end to end through the public API with host buffers
+    host_in = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in t.items()}
+    dev_in = {k: (torch.empty_like(v) if v is not None else None) for k, v in t.items()}
+    res = [x for x in (*out, *grads.values()) if x is not None]
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in res]
+    out_bytes = sum(x.numel() * x.element_size() for x in res)
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        for k, v in host_in.items():
+            if v is not None:
+                dev_in[k].copy_(v, non_blocking=True)
+        attn.forward(dev_in, out=out, stream=stream)
+        attn.backward(dev_in, out, grads=grads, stream=stream)
+        for hsrc, hdst in zip(res, host_out):
+            hdst.copy_(hsrc, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        x = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        e2e_ms = x.item()
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    pk = peaks()
+    bwd_avg = statistics.mean(bwd_ms)
+    fwd_avg = statistics.mean(fwd_ms)
+    achieved = w.useful_bwd_flops() / (bwd_avg * 1e-3) / 1e12
+    peak = pk["bf16_sustained"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(config, l2=f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB resident "
+                                  f"vs {L2_BYTES / 2**20:.0f} MiB L2); no flush"),
+        "pct_of_bf16_peak": value / world / pk["bf16_sustained"],
+        "fwd_ms": fwd_avg, "bwd_ms": bwd_avg,
+        "fwd_tflops": w.useful_fwd_flops() / (fwd_avg * 1e-3) / 1e12,
+        "bwd_tflops": achieved,
+        "roofline": {"bound": "tensor", "kernel": f"bwd_kernel<{w.d}> (csbp_attn_bwd call)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "peak_source": f"bf16_tflops_sustained of {pk['source']}",
+                     "traffic": None},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": in_bytes,
+                "d2h_bytes_per_step": out_bytes},
+        "gpu_launches": launches_per_step(w) * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+"""ctypes binding of libcsbp (include/csbp.h): argument marshalling only.
+
+Every step of the attention path runs in the library's kernels; PyTorch is
+used here only to own device memory and to name the current CUDA stream.
+There is no fallback: if libcsbp.so is missing or fails to load, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcsbp.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "csbp.h")
+
+OK = 0
+STATUS = {0: "CSBP_OK", -1: "CSBP_ERR_INVALID", -2: "CSBP_ERR_UNSUPPORTED",
+          -3: "CSBP_ERR_WORKSPACE", -4: "CSBP_ERR_CUDA", -5: "CSBP_ERR_TIMEOUT",
+          -6: "CSBP_ERR_CAPACITY"}
+
+
+class CsbpError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("L", ctypes.c_int32), ("M", ctypes.c_int32),
+                ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("P", ctypes.c_int32), ("tile_q", ctypes.c_int32), ("tile_kv", ctypes.c_int32),
+                ("has_clean_queries", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+class Inputs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")]
+
+
+class ScheduleInfo(ctypes.Structure):
+    _fields_ = [("n_fwd_tasks", ctypes.c_int32), ("n_fwd_segments", ctypes.c_int32),
+                ("n_bwd_tasks", ctypes.c_int32), ("n_bwd_segments", ctypes.c_int32),
+                ("tile_pairs", ctypes.c_int64), ("bytes", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libcsbp.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} not built: run block_diffusion_lm_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        L.csbp_block_schedule.argtypes = [P(Problem), P(i32), P(i32), vp, i64, P(ScheduleInfo)]
+        L.csbp_workspace_bytes.argtypes = [P(Problem), ctypes.c_int]
+        L.csbp_workspace_bytes.restype = sz
+        L.csbp_attn_fwd.argtypes = [P(Problem), P(Inputs), vp, P(ScheduleInfo), vp, vp, vp, vp,
+                                    sz, vp]
+        L.csbp_attn_bwd.argtypes = [P(Problem), P(Inputs), vp, P(ScheduleInfo), vp, vp, vp, vp,
+                                    vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.csbp_lse_merge.argtypes = [i32, P(vp), P(vp), i64, i32, i32, vp, vp, vp]
+        L.csbp_check_status.argtypes = [vp, vp]
+        L.csbp_status_string.argtypes = [ctypes.c_int]
+        L.csbp_status_string.restype = ctypes.c_char_p
+        L.csbp_version.restype = i32
+        for fn in ("csbp_block_schedule", "csbp_attn_fwd", "csbp_attn_bwd", "csbp_lse_merge",
+                   "csbp_check_status"):
+            getattr(L, fn).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def header_functions():
+    """Names of the functions include/csbp.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(csbp_\w+)\s*\(", text, re.M)))
+
+
+def _check(fn, status):
+    if status != OK:
+        raise CsbpError(fn, status)
+
+
+def make_problem(batch, L, M, Hq, Hkv, d, P=1, has_clean_queries=True, scale=None,
+                 tile=128) -> Problem:
+    return Problem(batch, L, M, Hq, Hkv, d, P, tile, tile, 1 if has_clean_queries else 0,
+                   float(scale if scale is not None else d ** -0.5))
+
+
+def block_schedule(problem: Problem):
+    """Host work list: returns (block_owner, chunk_owner, words[int32], info)."""
+    info = ScheduleInfo()
+    B = problem.L // problem.M if problem.M > 0 else 0
+    bo = np.zeros(max(B, 1), np.int32)
+    co = np.zeros(max(2 * problem.P, 1), np.int32)
+    st = lib().csbp_block_schedule(ctypes.byref(problem),
+                                   bo.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                   co.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                   None, 0, ctypes.byref(info))
+    if st != -6:
+        _check("csbp_block_schedule", st)
+    words = np.zeros(info.bytes // 4, np.int32)
+    st = lib().csbp_block_schedule(ctypes.byref(problem),
+                                   bo.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                   co.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                   words.ctypes.data_as(ctypes.c_void_p), words.nbytes,
+                                   ctypes.byref(info))
+    _check("csbp_block_schedule", st)
+    return bo[:B], co[:2 * problem.P], words, info
+
+
+def workspace_bytes(problem: Problem, which: int) -> int:
+    return int(lib().csbp_workspace_bytes(ctypes.byref(problem), which))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def attn_fwd(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse, workspace, stream=None):
+    inp = Inputs(*(_ptr(inputs.get(n)) for n in
+                   ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")))
+    st = lib().csbp_attn_fwd(ctypes.byref(problem), ctypes.byref(inp), _ptr(work_dev),
+                             ctypes.byref(info), _ptr(o_clean), _ptr(o_corr), _ptr(lse),
+                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream_ptr(stream))
+    _check("csbp_attn_fwd", st)
+
+
+def attn_bwd(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse, do_clean, do_corr,
+             grads: dict, workspace, stream=None):
+    inp = Inputs(*(_ptr(inputs.get(n)) for n in
+                   ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")))
+    st = lib().csbp_attn_bwd(ctypes.byref(problem), ctypes.byref(inp), _ptr(work_dev),
+                             ctypes.byref(info), _ptr(o_clean), _ptr(o_corr), _ptr(lse),
+                             _ptr(do_clean), _ptr(do_corr), _ptr(grads.get("dq_clean")),
+                             _ptr(grads["dq_corr"]), _ptr(grads["dk_clean"]),
+                             _ptr(grads["dv_clean"]), _ptr(grads["dk_corr"]),
+                             _ptr(grads["dv_corr"]), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check("csbp_attn_bwd", st)
+
+
+def lse_merge(o_parts, lse_parts, o_out, lse_out, stream=None):
+    """o_parts: list of fp32 [rows, Hq, d] device tensors; lse_parts: list of
+    fp32 [Hq, rows]; o_out bf16 [rows, Hq, d]; lse_out fp32 [Hq, rows]."""
+    n = len(o_parts)
+    rows, Hq, d = o_parts[0].shape
+    op = (ctypes.c_void_p * n)(*[t.data_ptr() for t in o_parts])
+    zp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in lse_parts])
+    st = lib().csbp_lse_merge(n, op, zp, rows, Hq, d, _ptr(o_out), _ptr(lse_out),
+                              _stream_ptr(stream))
+    _check("csbp_lse_merge", st)
+
+
+def check_status(workspace, stream=None):
+    st = lib().csbp_check_status(_ptr(workspace), _stream_ptr(stream))
+    _check("csbp_check_status", st)
+
+
+class BlockDiffusionAttention:
+    """Owns the device work list and workspaces of one problem shape.
+
+    forward(t) / backward(t, o) take dicts of bf16 [batch, L, H, d] CUDA
+    tensors (keys as in `inputs.make_inputs`) and return fresh outputs.
+    """
+
+    def __init__(self, batch, L, M, Hq, Hkv, d, P=1, has_clean_queries=True, scale=None,
+                 device="cuda"):
+        import torch
+        self.problem = make_problem(batch, L, M, Hq, Hkv, d, P, has_clean_queries, scale)
+        bo, co, words, info = block_schedule(self.problem)
+        self.block_owner, self.chunk_owner, self.info = bo, co, info
+        self.work_host = words
+        self.work_dev = torch.from_numpy(words).to(device)
+        self.ws_fwd = torch.zeros(workspace_bytes(self.problem, 0), dtype=torch.uint8, device=device)
+        self.ws_bwd = torch.zeros(workspace_bytes(self.problem, 1), dtype=torch.uint8, device=device)
+        self.device = device
+        self.shape = (batch, L, Hq, d)
+        self.kv_shape = (batch, L, Hkv, d)
+        self.has_clean = has_clean_queries
+
+    def alloc_outputs(self):
+        import torch
+        b, L, Hq, d = self.shape
+        o_clean = torch.empty(self.shape, dtype=torch.bfloat16, device=self.device) if self.has_clean else None
+        o_corr = torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
+        lse = torch.full((b, 2, Hq, L), float("nan"), dtype=torch.float32, device=self.device)
+        return o_clean, o_corr, lse
+
+    def alloc_grads(self):
+        import torch
+        g = {k: torch.empty(self.kv_shape, dtype=torch.bfloat16, device=self.device)
+             for k in ("dk_clean", "dv_clean", "dk_corr", "dv_corr")}
+        g["dq_corr"] = torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
+        g["dq_clean"] = (torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
+                         if self.has_clean else None)
+        return g
+
+    def forward(self, t, out=None, stream=None):
+        o_clean, o_corr, lse = out if out is not None else self.alloc_outputs()
+        attn_fwd(self.problem, t, self.work_dev, self.info, o_clean, o_corr, lse, self.ws_fwd,
+                 stream)
+        return o_clean, o_corr, lse
+
+    def backward(self, t, fwd_out, grads=None, stream=None):
+        o_clean, o_corr, lse = fwd_out
+        g = grads if grads is not None else self.alloc_grads()
+        attn_bwd(self.problem, t, self.work_dev, self.info, o_clean, o_corr, lse,
+                 t.get("do_clean"), t["do_corr"], g, self.ws_bwd, stream)
+        return g
+
+    def check(self, stream=None):
+        check_status(self.ws_fwd, stream)
+        check_status(self.ws_bwd, stream)

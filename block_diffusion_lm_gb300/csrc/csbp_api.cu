@@ -1,0 +1,332 @@
+// C-ABI entry points of libcsbp: argument validation, TMA descriptor
+// encoding, workspace carving and kernel launches.  No entry point allocates
+// memory; all device work goes to the caller's stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "csbp.h"
+#include "csbp_internal.h"
+
+namespace csbp {
+
+cudaError_t launch_fwd(int d, const CUtensorMap* maps, const FwdParams& p, int n_tasks,
+                       cudaStream_t stream);
+cudaError_t launch_bwd(int d, const CUtensorMap* maps, const BwdParams& p, int n_tasks,
+                       cudaStream_t stream);
+cudaError_t launch_lse_merge(const MergeArgs& a, int n_parts, int64_t rows, int Hq, int d,
+                             void* o_out, float* z_out, cudaStream_t stream);
+cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, float* Dsum, float* dq_acc,
+                           int64_t rows, int Hq, int L, cudaStream_t stream);
+cudaError_t launch_dq_convert(const float* acc, void* dq, int64_t n_elems, float scale,
+                              cudaStream_t stream);
+cudaError_t launch_fill(float* x, int64_t n, float v, cudaStream_t stream);
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D map over a bf16 [batch][L][H][d] tensor viewed as {H*d, L, batch};
+// box = 64 elements (128 B, one swizzle row) x 128 rows x 1.
+bool make_map(CUtensorMap* m, const void* base, int64_t H, int d, int64_t L, int64_t batch) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(H * d), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(H * d * 2),
+                           static_cast<cuuint64_t>(L * H * d * 2)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct WsLayout {
+  size_t status = 0, part_o = 0, part_lse = 0, dsum = 0, dq_acc = 0, total = 0;
+};
+
+WsLayout ws_layout(const csbp_problem* p, int which) {
+  WsLayout w;
+  const size_t rows = static_cast<size_t>(p->batch) * p->L;
+  size_t off = kStatusBytes;
+  if (which == 0) {
+    if (p->P > 1) {
+      w.part_o = off;
+      off += round256(static_cast<size_t>(p->P + 1) * 2 * rows * p->Hq * p->d * 4);
+      w.part_lse = off;
+      off += round256(static_cast<size_t>(p->P + 1) * 2 * rows * p->Hq * 4);
+    }
+  } else {
+    w.dsum = off;
+    off += round256(2 * rows * p->Hq * 4);
+    w.dq_acc = off;
+    off += round256(2 * rows * p->Hq * p->d * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+csbp_status check_inputs(const csbp_problem* p, const csbp_inputs* in) {
+  if (!in) return CSBP_ERR_INVALID;
+  if (!in->k_clean || !in->v_clean || !in->q_corr || !in->k_corr || !in->v_corr)
+    return CSBP_ERR_INVALID;
+  if (p->has_clean_queries && !in->q_clean) return CSBP_ERR_INVALID;
+  const void* ptrs[6] = {in->q_clean, in->k_clean, in->v_clean, in->q_corr, in->k_corr, in->v_corr};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return CSBP_ERR_INVALID;
+  return CSBP_OK;
+}
+
+// Offsets of the four record arrays, from the deterministic layout.
+struct WorkOffsets {
+  int64_t fwd_tasks, fwd_segs, bwd_tasks, bwd_segs;
+};
+
+WorkOffsets work_offsets(const csbp_schedule_info* info) {
+  WorkOffsets o;
+  o.fwd_tasks = kHeaderWords;
+  o.fwd_segs = o.fwd_tasks + static_cast<int64_t>(info->n_fwd_tasks) * kTaskWords;
+  o.bwd_tasks = o.fwd_segs + static_cast<int64_t>(info->n_fwd_segments) * kSegWords;
+  o.bwd_segs = o.bwd_tasks + static_cast<int64_t>(info->n_bwd_tasks) * kTaskWords;
+  return o;
+}
+
+}  // namespace
+
+}  // namespace csbp
+
+using namespace csbp;
+
+extern "C" int32_t csbp_version(void) { return 100; }
+
+extern "C" const char* csbp_status_string(csbp_status s) {
+  switch (s) {
+    case CSBP_OK: return "ok";
+    case CSBP_ERR_INVALID: return "invalid argument";
+    case CSBP_ERR_UNSUPPORTED: return "unsupported problem";
+    case CSBP_ERR_WORKSPACE: return "workspace too small";
+    case CSBP_ERR_CUDA: return "CUDA error";
+    case CSBP_ERR_TIMEOUT: return "device wait timed out";
+    case CSBP_ERR_CAPACITY: return "output buffer too small";
+  }
+  return "unknown status";
+}
+
+extern "C" size_t csbp_workspace_bytes(const csbp_problem* problem, int which) {
+  if (validate_problem(problem) != CSBP_OK || (which != 0 && which != 1)) return 0;
+  return ws_layout(problem, which).total;
+}
+
+extern "C" csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inputs* in,
+                                     const void* work_dev, const csbp_schedule_info* info,
+                                     void* o_clean, void* o_corr, float* lse, void* workspace,
+                                     size_t ws_bytes, void* stream_) {
+  csbp_status st = validate_problem(problem);
+  if (st != CSBP_OK) return st;
+  if (problem->tile_q != kTile) return CSBP_ERR_UNSUPPORTED;
+  if ((st = check_inputs(problem, in)) != CSBP_OK) return st;
+  if (!work_dev || !info || !o_corr || !lse || !workspace) return CSBP_ERR_INVALID;
+  if (problem->has_clean_queries && !o_clean) return CSBP_ERR_INVALID;
+  if (!aligned16(work_dev) || !aligned16(o_corr) || (o_clean && !aligned16(o_clean)) ||
+      !aligned16(lse) || !aligned16(workspace))
+    return CSBP_ERR_INVALID;
+  const WsLayout wl = ws_layout(problem, 0);
+  if (ws_bytes < wl.total) return CSBP_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const csbp_problem& p = *problem;
+
+  CUtensorMap maps[6];
+  const void* qc = in->q_clean ? in->q_clean : in->q_corr;  // unused map when absent
+  if (!make_map(&maps[0], qc, p.Hq, p.d, p.L, p.batch) ||
+      !make_map(&maps[1], in->q_corr, p.Hq, p.d, p.L, p.batch) ||
+      !make_map(&maps[2], in->k_clean, p.Hkv, p.d, p.L, p.batch) ||
+      !make_map(&maps[3], in->k_corr, p.Hkv, p.d, p.L, p.batch) ||
+      !make_map(&maps[4], in->v_clean, p.Hkv, p.d, p.L, p.batch) ||
+      !make_map(&maps[5], in->v_corr, p.Hkv, p.d, p.L, p.batch))
+    return CSBP_ERR_CUDA;
+
+  const WorkOffsets wo = work_offsets(info);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  FwdParams fp;
+  fp.tasks = static_cast<const int32_t*>(work_dev) + wo.fwd_tasks;
+  fp.segs = static_cast<const int32_t*>(work_dev) + wo.fwd_segs;
+  fp.L = p.L;
+  fp.M = p.M;
+  fp.Hq = p.Hq;
+  fp.Hkv = p.Hkv;
+  fp.G = p.Hq / p.Hkv;
+  fp.batch = p.batch;
+  fp.scale_log2 = p.scale * 1.4426950408889634f;
+  fp.o[0] = o_clean;
+  fp.o[1] = o_corr;
+  fp.lse = lse;
+  fp.part_o = nullptr;
+  fp.part_lse = nullptr;
+  fp.partial_mode = p.P > 1 ? 1 : 0;
+  fp.status = reinterpret_cast<int*>(ws + wl.status);
+  if (p.P > 1) {
+    fp.part_o = reinterpret_cast<float*>(ws + wl.part_o);
+    fp.part_lse = reinterpret_cast<float*>(ws + wl.part_lse);
+    const int64_t n_lse = static_cast<int64_t>(p.P + 1) * 2 * p.batch * p.Hq * p.L;
+    if (launch_fill(fp.part_lse, n_lse, -INFINITY, stream) != cudaSuccess) return CSBP_ERR_CUDA;
+  }
+  if (launch_fwd(p.d, maps, fp, info->n_fwd_tasks, stream) != cudaSuccess) return CSBP_ERR_CUDA;
+  if (p.P > 1) {
+    const int n_parts = p.P + 1;
+    const int64_t slab_o = static_cast<int64_t>(p.L) * p.Hq * p.d;
+    const int64_t slab_z = static_cast<int64_t>(p.Hq) * p.L;
+    for (int qs = p.has_clean_queries ? 0 : 1; qs < 2; ++qs) {
+      for (int bz = 0; bz < p.batch; ++bz) {
+        MergeArgs a;
+        for (int s = 0; s < n_parts; ++s) {
+          const int64_t prow = (static_cast<int64_t>(s) * 2 + qs) * p.batch + bz;
+          a.o[s] = fp.part_o + prow * slab_o;
+          a.z[s] = fp.part_lse + prow * slab_z;
+        }
+        void* oo = static_cast<uint16_t*>(qs ? o_corr : o_clean) + bz * slab_o;  // bf16 elements
+        float* zo = lse + (static_cast<int64_t>(bz) * 2 + qs) * slab_z;
+        if (launch_lse_merge(a, n_parts, p.L, p.Hq, p.d, oo, zo, stream) != cudaSuccess)
+          return CSBP_ERR_CUDA;
+      }
+    }
+  }
+  return CSBP_OK;
+}
+
+extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inputs* in,
+                                     const void* work_dev, const csbp_schedule_info* info,
+                                     const void* o_clean, const void* o_corr, const float* lse,
+                                     const void* do_clean, const void* do_corr, void* dq_clean,
+                                     void* dq_corr, void* dk_clean, void* dv_clean, void* dk_corr,
+                                     void* dv_corr, void* workspace, size_t ws_bytes,
+                                     void* stream_) {
+  csbp_status st = validate_problem(problem);
+  if (st != CSBP_OK) return st;
+  if (problem->tile_q != kTile) return CSBP_ERR_UNSUPPORTED;
+  if ((st = check_inputs(problem, in)) != CSBP_OK) return st;
+  const bool hc = problem->has_clean_queries != 0;
+  if (!work_dev || !info || !o_corr || !lse || !do_corr || !dq_corr || !dk_clean || !dv_clean ||
+      !dk_corr || !dv_corr || !workspace)
+    return CSBP_ERR_INVALID;
+  if (hc && (!o_clean || !do_clean || !dq_clean)) return CSBP_ERR_INVALID;
+  const void* all[] = {work_dev, o_corr, lse, do_corr, dq_corr, dk_clean, dv_clean, dk_corr,
+                       dv_corr, workspace, o_clean, do_clean, dq_clean};
+  for (const void* q : all)
+    if (q && !aligned16(q)) return CSBP_ERR_INVALID;
+  const WsLayout wl = ws_layout(problem, 1);
+  if (ws_bytes < wl.total) return CSBP_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const csbp_problem& p = *problem;
+
+  CUtensorMap maps[8];
+  const void* qc = in->q_clean ? in->q_clean : in->q_corr;
+  const void* dc = do_clean ? do_clean : do_corr;
+  if (!make_map(&maps[0], qc, p.Hq, p.d, p.L, p.batch) ||
+      !make_map(&maps[1], in->q_corr, p.Hq, p.d, p.L, p.batch) ||
+      !make_map(&maps[2], in->k_clean, p.Hkv, p.d, p.L, p.batch) ||
+      !make_map(&maps[3], in->k_corr, p.Hkv, p.d, p.L, p.batch) ||
+      !make_map(&maps[4], in->v_clean, p.Hkv, p.d, p.L, p.batch) ||
+      !make_map(&maps[5], in->v_corr, p.Hkv, p.d, p.L, p.batch) ||
+      !make_map(&maps[6], dc, p.Hq, p.d, p.L, p.batch) ||
+      !make_map(&maps[7], do_corr, p.Hq, p.d, p.L, p.batch))
+    return CSBP_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* dsum = reinterpret_cast<float*>(ws + wl.dsum);
+  float* dq_acc = reinterpret_cast<float*>(ws + wl.dq_acc);
+  const int64_t rows = static_cast<int64_t>(p.batch) * p.L;
+  const int64_t stream_elems = rows * p.Hq * p.d;
+  const void* o_s[2] = {o_clean, o_corr};
+  const void* do_s[2] = {do_clean, do_corr};
+  for (int qs = hc ? 0 : 1; qs < 2; ++qs) {
+    if (launch_bwd_pre(p.d, o_s[qs], do_s[qs], dsum + qs * rows * p.Hq, dq_acc + qs * stream_elems,
+                       rows, p.Hq, p.L, stream) != cudaSuccess)
+      return CSBP_ERR_CUDA;
+  }
+
+  const WorkOffsets wo = work_offsets(info);
+  BwdParams bp;
+  bp.tasks = static_cast<const int32_t*>(work_dev) + wo.bwd_tasks;
+  bp.segs = static_cast<const int32_t*>(work_dev) + wo.bwd_segs;
+  bp.L = p.L;
+  bp.M = p.M;
+  bp.Hq = p.Hq;
+  bp.Hkv = p.Hkv;
+  bp.G = p.Hq / p.Hkv;
+  bp.batch = p.batch;
+  bp.scale_log2 = p.scale * 1.4426950408889634f;
+  bp.scale = p.scale;
+  bp.lse = lse;
+  bp.Dsum = dsum;
+  bp.dq_acc = dq_acc;
+  bp.dk[0] = dk_clean;
+  bp.dk[1] = dk_corr;
+  bp.dv[0] = dv_clean;
+  bp.dv[1] = dv_corr;
+  bp.status = reinterpret_cast<int*>(ws + wl.status);
+  if (launch_bwd(p.d, maps, bp, info->n_bwd_tasks, stream) != cudaSuccess) return CSBP_ERR_CUDA;
+
+  void* dq_s[2] = {dq_clean, dq_corr};
+  for (int qs = hc ? 0 : 1; qs < 2; ++qs) {
+    if (launch_dq_convert(dq_acc + qs * stream_elems, dq_s[qs], stream_elems, p.scale, stream) !=
+        cudaSuccess)
+      return CSBP_ERR_CUDA;
+  }
+  return CSBP_OK;
+}
+
+extern "C" csbp_status csbp_lse_merge(int32_t n_parts, const float* const* o_parts,
+                                      const float* const* lse_parts, int64_t rows, int32_t Hq,
+                                      int32_t d, void* o_out, float* lse_out, void* stream) {
+  if (n_parts < 1 || n_parts > kMaxParts || rows < 1 || Hq < 1 || d < 4 || d % 4 != 0)
+    return CSBP_ERR_INVALID;
+  if (!o_parts || !lse_parts || !o_out || !lse_out) return CSBP_ERR_INVALID;
+  if (!aligned16(o_out) && (d % 8 != 0 || (reinterpret_cast<uintptr_t>(o_out) & 7u)))
+    return CSBP_ERR_INVALID;
+  MergeArgs a;
+  for (int s = 0; s < n_parts; ++s) {
+    if (!o_parts[s] || !lse_parts[s] || !aligned16(o_parts[s])) return CSBP_ERR_INVALID;
+    a.o[s] = o_parts[s];
+    a.z[s] = lse_parts[s];
+  }
+  if (launch_lse_merge(a, n_parts, rows, Hq, d, o_out, lse_out,
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CSBP_ERR_CUDA;
+  return CSBP_OK;
+}
+
+extern "C" csbp_status csbp_check_status(void* workspace, void* stream) {
+  if (!workspace) return CSBP_ERR_INVALID;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CSBP_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CSBP_ERR_CUDA;
+  if (v != 0) {
+    if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return CSBP_ERR_CUDA;
+    return CSBP_ERR_TIMEOUT;
+  }
+  return CSBP_OK;
+}

@@ -1,0 +1,63 @@
+// Internal declarations shared by the translation units of libcsbp.
+#pragma once
+
+#include <cstdint>
+
+#include "csbp.h"
+
+namespace csbp {
+
+constexpr int32_t kMagic = 0x43534250;  // 'CSBP'
+constexpr int32_t kVersion = 1;
+constexpr int kHeaderWords = 16;
+constexpr int kTaskWords = 8;
+constexpr int kSegWords = 4;
+constexpr int kMaxParts = 64;
+constexpr int kTile = 128;  // query and key tile rows of the kernels
+
+// Header word indices of a work list.
+enum HeaderWord {
+  H_MAGIC = 0, H_VERSION, H_L, H_M, H_TILE, H_P, H_HAS_CLEAN, H_N_FWD_TASKS,
+  H_N_FWD_SEGS, H_N_BWD_TASKS, H_N_BWD_SEGS, H_OFF_FWD_TASKS, H_OFF_FWD_SEGS,
+  H_OFF_BWD_TASKS, H_OFF_BWD_SEGS, H_TOTAL
+};
+
+csbp_status validate_problem(const csbp_problem* p);
+int classify_tile(int q_stream, int64_t qt, int k_stream, int64_t kt, int64_t L, int64_t M,
+                  int64_t T);
+
+// Launch-side parameter blocks (plain data, passed by value to kernels).
+struct FwdParams {
+  const int32_t* tasks;  // device: fwd task records
+  const int32_t* segs;   // device: fwd segment records
+  int32_t L, M, Hq, Hkv, G, batch;
+  float scale_log2;      // softmax scale * log2(e)
+  void* o[2];            // bf16 outputs per query stream
+  float* lse;            // [batch][2][Hq][L]
+  float* part_o;         // [(P+1)][2][batch][L][Hq][d] fp32 (partial mode)
+  float* part_lse;       // [(P+1)][2][batch][Hq][L]
+  int32_t partial_mode;
+  int* status;
+};
+
+// Per-part pointers of one LSE merge (o: [rows][Hq][d] fp32, z: [Hq][rows]).
+struct MergeArgs {
+  const float* o[kMaxParts];
+  const float* z[kMaxParts];
+};
+
+struct BwdParams {
+  const int32_t* tasks;  // device: bwd task records
+  const int32_t* segs;   // device: bwd segment records
+  int32_t L, M, Hq, Hkv, G, batch;
+  float scale_log2;
+  float scale;
+  const float* lse;      // [batch][2][Hq][L]
+  const float* Dsum;     // [2][batch][Hq][L]
+  float* dq_acc;         // [2][batch][L][Hq][d] fp32, pre-zeroed
+  void* dk[2];           // bf16 [batch][L][Hkv][d] per key stream
+  void* dv[2];
+  int* status;
+};
+
+}  // namespace csbp

@@ -1,0 +1,263 @@
+// Host-side ownership and mask-aware tile scheduling (csbp_block_schedule).
+//
+// Ownership follows the dual-end pairing of the "CSBP 完全拆解" blog, section
+// "负载均衡：为什么要首尾块配对", and the Turbo-dLLM project page, section "Load
+// balancing: pairing early and late blocks": the clean sequence is cut into
+// 2P contiguous chunks, shard r owns chunks r and 2P-1-r, and a corrupted
+// block belongs to the owner of the clean chunk holding its first position.
+//
+// The tile work list enumerates only the (query tile, key tile) pairs that
+// hold at least one entry allowed by the block-diffusion mask ("传统上下文并行
+// 为什么会传错东西" section of the same blog: a corrupted query of block b reads
+// its own block's corrupted keys and the clean keys of blocks < b; clean
+// queries read clean keys of blocks <= b).  Classification of a tile pair is
+// analytic on block-id intervals, so building the list is O(tiles^2) integer
+// work with no mask materialised.
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "csbp.h"
+#include "csbp_internal.h"
+
+namespace csbp {
+
+// 0 = no allowed entry, 1 = some (partial), 2 = all entries allowed.
+int classify_tile(int q_stream, int64_t qt, int k_stream, int64_t kt, int64_t L, int64_t M,
+                  int64_t T) {
+  const int64_t r0 = qt * T, r1 = std::min(r0 + T, L) - 1;
+  const int64_t c0 = kt * T, c1 = std::min(c0 + T, L) - 1;
+  if (r0 > r1 || c0 > c1) return 0;
+  const int64_t bq0 = r0 / M, bq1 = r1 / M, bk0 = c0 / M, bk1 = c1 / M;
+  if (q_stream == 0 && k_stream == 1) return 0;  // clean q never reads corrupted k
+  if (q_stream == 0) {                           // clean-clean: bk <= bq
+    if (bk0 > bq1) return 0;
+    return bk1 <= bq0 ? 2 : 1;
+  }
+  if (k_stream == 0) {  // corrupted q, clean k: bk < bq
+    if (bk0 >= bq1) return 0;
+    return bk1 < bq0 ? 2 : 1;
+  }
+  // corrupted q, corrupted k: bk == bq
+  if (bk1 < bq0 || bk0 > bq1) return 0;
+  return (bk0 == bk1 && bq0 == bq1 && bk0 == bq0) ? 2 : 1;
+}
+
+namespace {
+
+struct Seg {
+  int32_t stream, begin, end, flags;
+};
+struct Task {
+  int32_t a_stream, a_tile, part;
+  std::vector<Seg> segs;
+  int32_t cost;
+  int64_t canon;
+};
+
+// Append tile `t` with class `cls` (1/2) of `stream` to a run-length list of
+// homogeneous segments (same stream, same partial flag, same part).
+void push_tile(std::vector<Seg>& segs, std::vector<int32_t>& seg_part, int32_t stream,
+               int32_t t, int cls, int32_t part) {
+  const int32_t flags = (cls == 1) ? 1 : 0;
+  if (!segs.empty()) {
+    Seg& s = segs.back();
+    if (s.stream == stream && s.end == t && s.flags == flags && seg_part.back() == part) {
+      s.end = t + 1;
+      return;
+    }
+  }
+  segs.push_back({stream, t, t + 1, flags});
+  seg_part.push_back(part);
+}
+
+}  // namespace
+
+csbp_status validate_problem(const csbp_problem* p) {
+  if (!p) return CSBP_ERR_INVALID;
+  if (p->batch < 1 || p->L < 1 || p->M < 1 || p->Hq < 1 || p->Hkv < 1 || p->P < 1)
+    return CSBP_ERR_INVALID;
+  if (p->L % p->M != 0) return CSBP_ERR_INVALID;
+  if (p->Hq % p->Hkv != 0) return CSBP_ERR_INVALID;
+  if (!(p->scale > 0.0f) || p->scale != p->scale) return CSBP_ERR_INVALID;
+  if (p->tile_q < 1 || p->tile_kv < 1) return CSBP_ERR_INVALID;
+  if (p->has_clean_queries != 0 && p->has_clean_queries != 1) return CSBP_ERR_INVALID;
+  if (p->d != 64 && p->d != 128) return CSBP_ERR_UNSUPPORTED;
+  if (p->tile_q != p->tile_kv) return CSBP_ERR_UNSUPPORTED;
+  if (p->P > 1) {
+    const int64_t B = p->L / p->M;
+    if (B % (2 * p->P) != 0) return CSBP_ERR_UNSUPPORTED;
+    if ((p->L / (2 * p->P)) % p->tile_kv != 0) return CSBP_ERR_UNSUPPORTED;
+    if (p->P + 1 > kMaxParts) return CSBP_ERR_UNSUPPORTED;
+  }
+  return CSBP_OK;
+}
+
+}  // namespace csbp
+
+using namespace csbp;
+
+extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t* block_owner,
+                                           int32_t* chunk_owner, void* work, int64_t work_cap,
+                                           csbp_schedule_info* info) {
+  csbp_status st = validate_problem(problem);
+  if (st != CSBP_OK) return st;
+  if (!info) return CSBP_ERR_INVALID;
+  const int64_t L = problem->L, M = problem->M, T = problem->tile_q;
+  const int32_t P = problem->P;
+  const int64_t B = L / M;
+  const int64_t nT = (L + T - 1) / T;
+  if (nT > (int64_t)1 << 30) return CSBP_ERR_UNSUPPORTED;
+
+  // ---- ownership (P == 1: one shard owning both chunks)
+  std::vector<int32_t> co(2 * P);
+  for (int32_t r = 0; r < P; ++r) {
+    co[r] = r;
+    co[2 * P - 1 - r] = r;
+  }
+  const int64_t chunk_len = (P > 1) ? L / (2 * P) : 0;
+  auto clean_part = [&](int64_t pos) -> int32_t {
+    if (P == 1) return 0;
+    return co[pos / chunk_len];
+  };
+  if (chunk_owner) std::memcpy(chunk_owner, co.data(), sizeof(int32_t) * 2 * P);
+  if (block_owner) {
+    for (int64_t b = 0; b < B; ++b) {
+      if (P == 1) {
+        block_owner[b] = 0;
+      } else {
+        block_owner[b] = co[(b * M) / chunk_len];
+      }
+    }
+  }
+
+  // ---- forward tasks: per query tile (P == 1, fused) or per (tile, part)
+  const int n_qs = problem->has_clean_queries ? 2 : 1;
+  const int q_stream0 = problem->has_clean_queries ? 0 : 1;
+  std::vector<Task> fwd;
+  int64_t pairs = 0;
+  for (int qs = q_stream0; qs < 2; ++qs) {
+    for (int64_t qt = 0; qt < nT; ++qt) {
+      std::vector<Seg> segs;
+      std::vector<int32_t> seg_part;
+      for (int ks = 0; ks < 2; ++ks) {
+        for (int64_t kt = 0; kt < nT; ++kt) {
+          const int cls = classify_tile(qs, qt, ks, kt, L, M, T);
+          if (!cls) continue;
+          ++pairs;
+          const int32_t part = (ks == 1) ? P : clean_part(kt * T);
+          push_tile(segs, seg_part, ks, (int32_t)kt, cls, part);
+        }
+      }
+      if (P == 1) {
+        Task t{qs, (int32_t)qt, -1, segs, 0, 0};
+        for (auto& s : segs) t.cost += s.end - s.begin;
+        t.canon = ((int64_t)qs * nT + qt);
+        fwd.push_back(std::move(t));
+      } else {
+        for (int32_t part = 0; part <= P; ++part) {
+          Task t{qs, (int32_t)qt, part, {}, 0, 0};
+          for (size_t i = 0; i < segs.size(); ++i)
+            if (seg_part[i] == part) {
+              t.segs.push_back(segs[i]);
+              t.cost += segs[i].end - segs[i].begin;
+            }
+          if (t.segs.empty()) continue;
+          t.canon = ((int64_t)qs * nT + qt) * (P + 1) + part;
+          fwd.push_back(std::move(t));
+        }
+      }
+    }
+  }
+  (void)n_qs;
+
+  // ---- backward tasks: per key tile, segments over query tiles
+  std::vector<Task> bwd;
+  for (int ks = 0; ks < 2; ++ks) {
+    for (int64_t kt = 0; kt < nT; ++kt) {
+      Task t{ks, (int32_t)kt, (ks == 1) ? P : clean_part(kt * T), {}, 0, 0};
+      std::vector<int32_t> dummy_part;
+      for (int qs = q_stream0; qs < 2; ++qs) {
+        // only a band of query tiles can read key tile kt; scan all for clarity
+        for (int64_t qt = 0; qt < nT; ++qt) {
+          const int cls = classify_tile(qs, qt, ks, kt, L, M, T);
+          if (!cls) continue;
+          push_tile(t.segs, dummy_part, qs, (int32_t)qt, cls, 0);
+          t.cost += 1;
+        }
+      }
+      // emitted even when no query reads the tile: its dK/dV are then zero
+      t.canon = (int64_t)ks * nT + kt;
+      bwd.push_back(std::move(t));
+    }
+  }
+
+  auto heavy_first = [](const Task& a, const Task& b) {
+    if (a.cost != b.cost) return a.cost > b.cost;
+    return a.canon < b.canon;
+  };
+  std::sort(fwd.begin(), fwd.end(), heavy_first);
+  std::sort(bwd.begin(), bwd.end(), heavy_first);
+
+  int64_t n_fseg = 0, n_bseg = 0;
+  for (auto& t : fwd) n_fseg += (int64_t)t.segs.size();
+  for (auto& t : bwd) n_bseg += (int64_t)t.segs.size();
+  const int64_t off_ft = kHeaderWords;
+  const int64_t off_fs = off_ft + (int64_t)fwd.size() * kTaskWords;
+  const int64_t off_bt = off_fs + n_fseg * kSegWords;
+  const int64_t off_bs = off_bt + (int64_t)bwd.size() * kTaskWords;
+  const int64_t total = off_bs + n_bseg * kSegWords;
+  if (total > INT32_MAX) return CSBP_ERR_UNSUPPORTED;
+
+  info->n_fwd_tasks = (int32_t)fwd.size();
+  info->n_fwd_segments = (int32_t)n_fseg;
+  info->n_bwd_tasks = (int32_t)bwd.size();
+  info->n_bwd_segments = (int32_t)n_bseg;
+  info->tile_pairs = pairs;
+  info->bytes = total * (int64_t)sizeof(int32_t);
+  if (!work || work_cap < info->bytes) return CSBP_ERR_CAPACITY;
+
+  int32_t* w = static_cast<int32_t*>(work);
+  std::memset(w, 0, (size_t)info->bytes);
+  const int32_t hdr[kHeaderWords] = {kMagic,
+                                     kVersion,
+                                     problem->L,
+                                     problem->M,
+                                     (int32_t)T,
+                                     P,
+                                     problem->has_clean_queries,
+                                     (int32_t)fwd.size(),
+                                     (int32_t)n_fseg,
+                                     (int32_t)bwd.size(),
+                                     (int32_t)n_bseg,
+                                     (int32_t)off_ft,
+                                     (int32_t)off_fs,
+                                     (int32_t)off_bt,
+                                     (int32_t)off_bs,
+                                     (int32_t)total};
+  std::memcpy(w, hdr, sizeof(hdr));
+  auto emit = [&](const std::vector<Task>& tasks, int64_t off_t, int64_t off_s) {
+    int64_t s = 0;
+    for (size_t i = 0; i < tasks.size(); ++i) {
+      const Task& t = tasks[i];
+      int32_t* tw = w + off_t + (int64_t)i * kTaskWords;
+      tw[0] = t.a_stream;
+      tw[1] = t.a_tile;
+      tw[2] = t.part;
+      tw[3] = (int32_t)s;
+      tw[4] = (int32_t)t.segs.size();
+      tw[5] = t.cost;
+      for (const Seg& g : t.segs) {
+        int32_t* sw = w + off_s + s * kSegWords;
+        sw[0] = g.stream;
+        sw[1] = g.begin;
+        sw[2] = g.end;
+        sw[3] = g.flags;
+        ++s;
+      }
+    }
+  };
+  emit(fwd, off_ft, off_fs);
+  emit(bwd, off_bt, off_bs);
+  return CSBP_OK;
+}

@@ -1,0 +1,195 @@
+/*
+ * csbp.h -- C ABI of libcsbp: two-copy block-diffusion attention, forward and
+ * backward, on one sm_103a GPU, with the per-rank math of context-sharded
+ * block parallelism (CSBP) run as virtual clean shards.
+ *
+ * Method (sources, cited by page title and section):
+ *  - "CSBP 完全拆解：块并行如何让长上下文扩散语言模型少传无效 KV" (blog),
+ *    section "传统上下文并行为什么会传错东西": the input is a clean copy and a
+ *    corrupted copy of a length-L sequence cut into B = L/M blocks; a
+ *    corrupted query of block b reads exactly [K_b; K^clean_<b] and
+ *    [V_b; V^clean_<b]; O = softmax(Q K^T / sqrt(d_h) + mask) V.
+ *  - same blog, section "CSBP：BP 管损坏块，CP 管干净上下文": forward
+ *    O_b = Attn(Q_b, [K_b; K^clean_<b], [V_b; V^clean_<b]); corrupted dQ/dK/dV
+ *    stay with the block owner, clean dK/dV accumulate to the clean-shard owner.
+ *  - same blog, section "在线 softmax 合并：为什么分两段算仍是同一个注意力":
+ *    partial outputs over disjoint key sets merge exactly by log-sum-exp.
+ *  - same blog, section "负载均衡：为什么要首尾块配对", and the Turbo-dLLM project
+ *    page "Block Parallelism for Efficient Distributed Long-Context Diffusion
+ *    Language Model Training", section "Load balancing: pairing early and late
+ *    blocks": block b and block B+1-b share a rank; the clean sequence is
+ *    sharded with the same early/late (zigzag) pairing.
+ * Readings where the pages are silent: clean queries attend block-causally
+ * over the clean copy and never read corrupted keys; query head h uses KV
+ * head h / (Hq/Hkv); LSE is the natural log of the softmax denominator.
+ *
+ * Conventions for every entry point:
+ *  - Memory is owned by the caller.  The library never allocates or frees
+ *    device memory and keeps no state across calls except a per-process
+ *    cache of the driver entry point used to encode TMA descriptors.
+ *  - Device work is enqueued asynchronously on `stream` (a cudaStream_t
+ *    passed as void*; NULL = legacy default stream).  Pointers named *_dev
+ *    or documented as "device" must be device (or managed) memory of the
+ *    current CUDA device.
+ *  - Tensors are bf16, contiguous, layout [batch][L][heads][d] unless stated.
+ *    Every device pointer must be 16-byte aligned.
+ *  - Errors are reported only as csbp_status values; arguments are validated
+ *    before anything is enqueued, so an error return enqueues no work.  A
+ *    device-side wait that exceeds its time budget (a hang guard, never
+ *    expected) makes the kernel drain and return; csbp_check_status reports
+ *    it afterwards as CSBP_ERR_TIMEOUT.
+ */
+#ifndef CSBP_H_
+#define CSBP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSBP_OK = 0,
+  CSBP_ERR_INVALID = -1,     /* bad argument (null, shape, alignment)        */
+  CSBP_ERR_UNSUPPORTED = -2, /* valid problem the kernels do not cover       */
+  CSBP_ERR_WORKSPACE = -3,   /* workspace smaller than csbp_workspace_bytes  */
+  CSBP_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed            */
+  CSBP_ERR_TIMEOUT = -5,     /* a bounded device wait gave up                */
+  CSBP_ERR_CAPACITY = -6     /* output buffer too small; size reported       */
+} csbp_status;
+
+/* Problem description.
+ *  L      clean length = corrupted length (positions per copy), L % M == 0
+ *  M      block size (B = L / M blocks)
+ *  Hq,Hkv query / key-value heads, Hq % Hkv == 0 (GQA group G = Hq / Hkv)
+ *  d      head dimension: 64 or 128
+ *  P      virtual clean shards: 1 = unsharded fused path; P > 1 = one partial
+ *         per clean shard plus the corrupted own-block partial, LSE-merged.
+ *         P > 1 needs (L/M) % (2P) == 0 and (L/(2P)) % tile_kv == 0.
+ *  tile_q, tile_kv  schedule granularity; the kernels need 128 / 128.
+ *  has_clean_queries  1 = both copies query; 0 = corrupted queries only
+ *         (drafter workload; clean K/V are context only).
+ *  scale  softmax scale (1/sqrt(d) for the standard layer).            */
+typedef struct {
+  int32_t batch, L, M, Hq, Hkv, d, P;
+  int32_t tile_q, tile_kv;
+  int32_t has_clean_queries;
+  float scale;
+} csbp_problem;
+
+/* Device input tensors, bf16 [batch][L][H][d] contiguous (H = Hq for q,
+ * Hkv for k/v).  q_clean may be NULL when has_clean_queries == 0.        */
+typedef struct {
+  const void *q_clean, *k_clean, *v_clean;
+  const void *q_corr, *k_corr, *v_corr;
+} csbp_inputs;
+
+/* Summary of a work list built by csbp_block_schedule. */
+typedef struct {
+  int32_t n_fwd_tasks;    /* forward tasks (one query tile [x part])      */
+  int32_t n_fwd_segments; /* key-tile ranges of the forward tasks         */
+  int32_t n_bwd_tasks;    /* backward tasks (one key tile)                */
+  int32_t n_bwd_segments; /* query-tile ranges of the backward tasks      */
+  int64_t tile_pairs;     /* (query tile, key tile) pairs with >=1 allowed entry */
+  int64_t bytes;          /* size of the work list                        */
+} csbp_schedule_info;
+
+/* Work-list layout (int32 words; produced and consumed only by this library
+ * but documented for tests):
+ *   words[0..15]  header: magic 0x43534250, version 1, L, M, tile, P,
+ *                 has_clean_queries, n_fwd_tasks, n_fwd_segments,
+ *                 n_bwd_tasks, n_bwd_segments, off_fwd_tasks, off_fwd_segs,
+ *                 off_bwd_tasks, off_bwd_segs, total_words
+ *   fwd task (8 words): q_stream, q_tile, part (-1 = all parts, fused),
+ *                 seg_begin, seg_count, kv_tiles, 0, 0
+ *   fwd segment (4 words): kv_stream, kv_tile_begin, kv_tile_end (exclusive),
+ *                 flags (bit0 = partial: tiles need the in-tile mask)
+ *   bwd task (8 words): kv_stream, kv_tile, part, seg_begin, seg_count,
+ *                 q_tiles, 0, 0  (one per key tile of both copies, including
+ *                 tiles no query reads, whose dK/dV are zero)
+ *   bwd segment (4 words): q_stream, q_tile_begin, q_tile_end, flags
+ * Streams: 0 = clean copy, 1 = corrupted copy.  Part of a key tile: the
+ * owner shard of its clean chunk (clean keys) or P (corrupted keys).
+ * Tasks are ordered heaviest first (ties in canonical order).            */
+
+/* Build the dual-end block ownership, the zigzag clean-chunk ownership and
+ * the mask-aware tile work list on the host (no CUDA call).
+ *  block_owner  host int32[B] or NULL: owner shard of each corrupted block
+ *  chunk_owner  host int32[2P] or NULL: owner shard of each clean chunk
+ *  work         host buffer for the work list, or NULL to query the size
+ *  work_cap     capacity of `work` in bytes
+ *  info         out: counts and the required size in bytes (always filled
+ *               on CSBP_OK and CSBP_ERR_CAPACITY)
+ * Shard r owns clean chunks r and 2P-1-r of the 2P contiguous chunks of
+ * length L/(2P); a corrupted block is owned by the owner of the chunk that
+ * holds its first position (so blocks b and B-1-b pair up, 0-based).
+ * Returns CSBP_ERR_CAPACITY if work is NULL or too small.               */
+csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t* block_owner,
+                                int32_t* chunk_owner, void* work, int64_t work_cap,
+                                csbp_schedule_info* info);
+
+/* Bytes of device workspace needed: which = 0 forward, 1 backward.
+ * Forward: a status word, plus for P > 1 the fp32 partials
+ *   (P+1) x 2 x batch x L x Hq x (d + 1) x 4 bytes.
+ * Backward: a status word, D (2 x batch x Hq x L fp32) and the fp32 dQ
+ *   accumulator (2 x batch x L x Hq x d).  Returns 0 for an invalid problem. */
+size_t csbp_workspace_bytes(const csbp_problem* problem, int which);
+
+/* Forward.  work_dev: device copy of the work list from csbp_block_schedule
+ * for this problem (info: its summary).  Outputs (device):
+ *   o_clean, o_corr  bf16 [batch][L][Hq][d]  (o_clean ignored, may be NULL,
+ *                    when has_clean_queries == 0)
+ *   lse              fp32 [batch][2][Hq][L], natural-log softmax denominator
+ *                    of each query row (copy 0 untouched without clean queries)
+ * P == 1: one fused pass per query tile over all its allowed key tiles.
+ * P > 1: per-part partial attention into the workspace, then the LSE merge.
+ * workspace: device, >= csbp_workspace_bytes(problem, 0).               */
+csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inputs* in,
+                          const void* work_dev, const csbp_schedule_info* info,
+                          void* o_clean, void* o_corr, float* lse, void* workspace,
+                          size_t ws_bytes, void* stream);
+
+/* Backward (exact): given the forward's O and LSE and the upstream dO,
+ * writes dQ for each query copy and dK, dV for each key copy (bf16, same
+ * layouts as the inputs; dK/dV summed over the G query heads of each KV
+ * head; outputs are overwritten, not accumulated).  Clean dK/dV collect
+ * contributions from clean queries of the same or later blocks and from
+ * corrupted queries of later blocks; corrupted dK/dV only from queries of
+ * their own block.  do_clean / dq_clean may be NULL without clean queries.
+ * workspace: device, >= csbp_workspace_bytes(problem, 1).               */
+csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inputs* in,
+                          const void* work_dev, const csbp_schedule_info* info,
+                          const void* o_clean, const void* o_corr, const float* lse,
+                          const void* do_clean, const void* do_corr, void* dq_clean,
+                          void* dq_corr, void* dk_clean, void* dv_clean, void* dk_corr,
+                          void* dv_corr, void* workspace, size_t ws_bytes, void* stream);
+
+/* Exact log-sum-exp merge of n_parts partial attentions over disjoint key
+ * sets (blog section "在线 softmax 合并"): m = max_s z_s, w_s = exp(z_s - m),
+ * O = sum_s w_s O_s / sum_s w_s, z = m + log(sum_s w_s), all in fp32; a part
+ * with z = -inf read no key and has weight 0.
+ *  o_parts   host array of n_parts device pointers, fp32 [rows][Hq][d]
+ *  lse_parts host array of n_parts device pointers, fp32 [Hq][rows]
+ *  o_out     device bf16 [rows][Hq][d];  lse_out device fp32 [Hq][rows]
+ * 1 <= n_parts <= 64, d % 4 == 0.                                        */
+csbp_status csbp_lse_merge(int32_t n_parts, const float* const* o_parts,
+                           const float* const* lse_parts, int64_t rows, int32_t Hq,
+                           int32_t d, void* o_out, float* lse_out, void* stream);
+
+/* Synchronise `stream`, then read and clear the device status word kept at
+ * the start of `workspace` by csbp_attn_fwd / csbp_attn_bwd.  Returns
+ * CSBP_ERR_TIMEOUT if a bounded device wait gave up since the last check. */
+csbp_status csbp_check_status(void* workspace, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* csbp_status_string(csbp_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t csbp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSBP_H_ */

@@ -432,34 +432,49 @@ def tile_pairs(L, M, Tq, Tkv, P=1, has_clean_queries=True):
 # --------------------------------------------------------------------------
 # Row / key sampled evaluation for long sequences
 # --------------------------------------------------------------------------
+def _kv_of_head(kc, kx, vc, vx, g):
+    K = np.concatenate([np.asarray(kc[:, g], np.float64), np.asarray(kx[:, g], np.float64)], 0)
+    V = np.concatenate([np.asarray(vc[:, g], np.float64), np.asarray(vx[:, g], np.float64)], 0)
+    return K, V
+
+
+def _gather_rows(qc, qx, doc, dox, rows, h):
+    """Query and dO vectors of rows [(q_stream, i)] for query head h."""
+    q = np.stack([np.asarray((qc if qs == CLEAN else qx)[i, h], np.float64) for qs, i in rows])
+    do = np.stack([np.asarray((doc if qs == CLEAN else dox)[i, h], np.float64) for qs, i in rows])
+    return q, do
+
+
 def sampled_rows(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples):
     """Exact O, lse, D and dQ for sampled query rows.
 
     samples: iterable of (q_stream, i, h).  Each row depends only on itself,
-    the full K/V of its KV head and dO_i.  Returns dict keyed by the sample
-    tuple -> (o [d], lse, D, dq [d]).
+    the full K/V of its KV head and dO_i, so the sampled rows of one head go
+    through `masked_attention` / `masked_attention_bwd` together with their
+    own mask rows.  Returns dict keyed by the sample tuple ->
+    (o [d], lse, D, dq [d]).
     """
     L, Hkv, d = np.shape(kc)
     Hq = np.shape(qx)[1]
     G = Hq // Hkv
-    out = {}
-    kcache = {}
+    by_head = {}
     for (qs, i, h) in samples:
-        g = h // G
-        if g not in kcache:
-            kcache[g] = (np.concatenate([np.asarray(kc[:, g], np.float64),
-                                         np.asarray(kx[:, g], np.float64)], 0),
-                         np.concatenate([np.asarray(vc[:, g], np.float64),
-                                         np.asarray(vx[:, g], np.float64)], 0))
-        K, V = kcache[g]
-        row = mask_row(qs, i, L, M)
-        q = np.asarray((qc if qs == CLEAN else qx)[i, h], np.float64)[None, :]
-        do = np.asarray((doc if qs == CLEAN else dox)[i, h], np.float64)[None, :]
-        Ks, Vs = K[row], V[row]
-        o, z = masked_attention(q, Ks, Vs, np.ones((1, Ks.shape[0]), bool), scale)
-        dq, _, _, D = masked_attention_bwd(q, Ks, Vs, np.ones((1, Ks.shape[0]), bool),
-                                           scale, do)
-        out[(qs, i, h)] = (o[0], float(z[0]), float(D[0]), dq[0])
+        by_head.setdefault(h, []).append((qs, i))
+    out = {}
+    for g in range(Hkv):
+        heads = [h for h in range(g * G, (g + 1) * G) if h in by_head]
+        if not heads:
+            continue
+        K, V = _kv_of_head(kc, kx, vc, vx, g)
+        for h in heads:
+            rows = by_head[h]
+            q, do = _gather_rows(qc, qx, doc, dox, rows, h)
+            allow = np.stack([mask_row(qs, i, L, M) for qs, i in rows])
+            o, z = masked_attention(q, K, V, allow, scale)
+            dq, _, _, D = masked_attention_bwd(q, K, V, allow, scale, do)
+            for r, (qs, i) in enumerate(rows):
+                out[(qs, i, h)] = (o[r], float(z[r]), float(D[r]), dq[r])
+        del K, V
     return out
 
 
@@ -477,37 +492,39 @@ def readers_of_key(k_stream, j, L, M, has_clean_queries=True):
 
 
 def sampled_keys(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples):
-    """Exact dK, dV for sampled keys (k_stream, j, g): sums over every reader
-    row of the G query heads of KV head g, each reader's P_ij and dS_ij taken
-    from that row's own full softmax."""
+    """Exact dK, dV for sampled keys (k_stream, j, g).
+
+    dK_j and dV_j sum over every query row that reads key j, over the G query
+    heads of KV head g.  The union of the sampled keys' readers goes through
+    `masked_attention_bwd` with each row's full mask (so every reader's P and
+    dS come from its own complete softmax); the sampled columns of its dK/dV
+    are then exact, because no other row reads those keys.  Keys with many
+    readers (early clean keys) are expensive; sample late or corrupted keys.
+    """
     L, Hkv, d = np.shape(kc)
     Hq = np.shape(qx)[1]
     G = Hq // Hkv
     has_clean = qc is not None
-    out = {}
+    by_g = {}
     for (ks, j, g) in samples:
-        K = np.concatenate([np.asarray(kc[:, g], np.float64), np.asarray(kx[:, g], np.float64)], 0)
-        V = np.concatenate([np.asarray(vc[:, g], np.float64), np.asarray(vx[:, g], np.float64)], 0)
-        col = ks * L + j
-        dk = np.zeros(d)
-        dv = np.zeros(d)
-        for (qs, i) in readers_of_key(ks, j, L, M, has_clean):
-            row = mask_row(qs, i, L, M)
+        by_g.setdefault(g, []).append((ks, j))
+    out = {}
+    for g, keys in by_g.items():
+        readers = sorted({r for ks, j in keys for r in readers_of_key(ks, j, L, M, has_clean)})
+        K, V = _kv_of_head(kc, kx, vc, vx, g)
+        dk = np.zeros((len(keys), d))
+        dv = np.zeros((len(keys), d))
+        cols = [ks * L + j for ks, j in keys]
+        if readers:
+            allow = np.stack([mask_row(qs, i, L, M) for qs, i in readers])
             for h in range(g * G, (g + 1) * G):
-                q = np.asarray((qc if qs == CLEAN else qx)[i, h], np.float64)[None, :]
-                do = np.asarray((doc if qs == CLEAN else dox)[i, h], np.float64)[None, :]
-                s = scale * (q @ K[row].T)[0]
-                m = s.max()
-                e = np.exp(s - m)
-                p_row = e / e.sum()
-                dp_row = (do @ V[row].T)[0]
-                D = float((p_row * dp_row).sum())
-                idx = int(np.flatnonzero(np.flatnonzero(row) == col)[0])
-                p = p_row[idx]
-                ds = p * (dp_row[idx] - D)
-                dv += p * do[0]
-                dk += scale * ds * q[0]
-        out[(ks, j, g)] = (dk, dv)
+                q, do = _gather_rows(qc, qx, doc, dox, readers, h)
+                _, dk_all, dv_all, _ = masked_attention_bwd(q, K, V, allow, scale, do)
+                dk += dk_all[cols]
+                dv += dv_all[cols]
+        for n, (ks, j) in enumerate(keys):
+            out[(ks, j, g)] = (dk[n], dv[n])
+        del K, V
     return out
 
 

@@ -1,0 +1,191 @@
+"""GPU parity: the CUDA path through the C-ABI against the float64 oracle.
+
+Tolerances (bf16 inputs, fp32 accumulation): O max-abs <= 1e-2; dQ, dK, dV
+relative Frobenius <= 1e-2; LSE abs <= 1e-3.  Small cases compare every
+element; the full-size workloads compare seeded samples of query rows (O,
+LSE, dQ) and of keys (dK, dV) that the oracle computes one by one, plus the
+exact whole-tensor invariants sum_j dK_j = 0 and sum_j dV_j = sum dO.
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_lm_gb300 import csbp
+from block_diffusion_lm_gb300.inputs import WORKLOADS, Workload, make_inputs, to_f64
+from oracle import csbp_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = 1e-2
+TOL_REL = 1e-2
+TOL_LSE = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from block_diffusion_lm_gb300 import build
+    build.build()
+
+
+def rel_fro(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def run_gpu(w: Workload, L=None, seed=None, P=None):
+    L = w.L if L is None else L
+    t = make_inputs(w, "cuda", seed=seed, L=L)
+    attn = csbp.BlockDiffusionAttention(w.batch, L, w.M, w.Hq, w.Hkv, w.d,
+                                        P=w.P if P is None else P,
+                                        has_clean_queries=w.has_clean_queries)
+    out = attn.forward(t)
+    g = attn.backward(t, out)
+    attn.check()
+    torch.cuda.synchronize()
+    return t, out, g
+
+
+SMALL = [
+    WORKLOADS["tiny"],
+    Workload("gqa_ragged", 1, 400, 16, 4, 2, 128, seed=11),
+    Workload("batch2", 2, 384, 32, 2, 1, 128, seed=12),
+    Workload("drafter_small", 1, 512, 16, 4, 1, 128, has_clean_queries=False, seed=13),
+    Workload("block_eq_tile", 1, 512, 128, 2, 2, 64, seed=14),
+    Workload("block_gt_tile", 1, 512, 256, 2, 1, 128, seed=15),
+    Workload("token_blocks", 1, 256, 1, 2, 2, 64, seed=16),
+    Workload("kscale", 1, 384, 32, 4, 1, 128, k_scale_range=(0.5, 2.0), seed=17),
+    Workload("single_partial_tile", 1, 48, 16, 2, 1, 128, seed=18),
+    Workload("sharded_small", 1, 1024, 16, 4, 2, 128, P=2, seed=19),
+    Workload("sharded_p4", 1, 2048, 32, 2, 1, 128, P=4, seed=20),
+    Workload("drafter_sharded", 1, 1024, 16, 2, 1, 64, P=2, has_clean_queries=False, seed=21),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_small_cases_match_oracle_elementwise(w):
+    t, (oc, ox, lse), g = run_gpu(w)
+    for b in range(w.batch):
+        f = {k: (to_f64(v[b]) if v is not None else None) for k, v in t.items()}
+        Oc, Ox, Z = O.bd_attention_fwd(f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"],
+                                       f["k_corr"], f["v_corr"], w.M, w.scale)
+        G = O.bd_attention_bwd(f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"],
+                               f["k_corr"], f["v_corr"], f["do_clean"], f["do_corr"], w.M, w.scale)
+        gl = to_f64(lse[b])
+        assert np.abs(to_f64(ox[b]) - Ox).max() <= TOL_O
+        assert np.abs(gl[1] - Z[1]).max() <= TOL_LSE
+        if w.has_clean_queries:
+            assert np.abs(to_f64(oc[b]) - Oc).max() <= TOL_O
+            assert np.abs(gl[0] - Z[0]).max() <= TOL_LSE
+            assert rel_fro(to_f64(g["dq_clean"][b]), G["dq_clean"]) <= TOL_REL
+        assert rel_fro(to_f64(g["dq_corr"][b]), G["dq_corr"]) <= TOL_REL
+        for k in ("dk_clean", "dv_clean", "dk_corr", "dv_corr"):
+            want = G[k]
+            got = to_f64(g[k][b])
+            if np.linalg.norm(want) == 0:
+                assert np.abs(got).max() == 0, k
+            else:
+                assert rel_fro(got, want) <= TOL_REL, (k, rel_fro(got, want))
+
+
+def test_sharded_equals_unsharded_on_gpu():
+    """Per-shard partials + LSE merge (P=4) reproduce the fused unsharded pass."""
+    w = Workload("shard_vs_fused", 1, 2048, 16, 4, 2, 128, P=4, seed=30)
+    _, (oc1, ox1, z1), g1 = run_gpu(w, P=1)
+    _, (oc4, ox4, z4), g4 = run_gpu(w, P=4)
+    assert (ox1.float() - ox4.float()).abs().max().item() <= 2 ** -7
+    assert (oc1.float() - oc4.float()).abs().max().item() <= 2 ** -7
+    assert (z1 - z4).abs().max().item() <= 1e-4
+    for k in ("dq_clean", "dq_corr", "dk_clean", "dv_clean", "dk_corr", "dv_corr"):
+        a, b = g1[k].double(), g4[k].double()
+        assert ((a - b).norm() / b.norm()).item() <= 1e-2, k
+
+
+def test_repeat_calls_are_deterministic_in_forward():
+    w = Workload("repeat", 1, 512, 32, 2, 1, 128, seed=31)
+    t = make_inputs(w, "cuda")
+    attn = csbp.BlockDiffusionAttention(1, 512, 32, 2, 1, 128)
+    a = attn.forward(t)
+    b = attn.forward(t)
+    torch.cuda.synchronize()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[0], b[0]) and torch.equal(a[2], b[2])
+
+
+# ------------------------------------------------------------------ full size
+def _invariants(w, t, g):
+    """sum_j dK_j = 0 per KV head; sum_j dV_j = sum of the group's dO rows."""
+    G = w.Hq // w.Hkv
+    dk = g["dk_clean"].double().sum(dim=1) + g["dk_corr"].double().sum(dim=1)  # [b, Hkv, d]
+    dv = g["dv_clean"].double().sum(dim=1) + g["dv_corr"].double().sum(dim=1)
+    do = t["do_corr"].double().sum(dim=1)
+    if t["do_clean"] is not None:
+        do = do + t["do_clean"].double().sum(dim=1)
+    do = do.view(w.batch, w.Hkv, G, w.d).sum(dim=2)
+    dk_scale = g["dk_clean"].double().abs().sum(dim=1).max().item()
+    assert dk.abs().max().item() <= 2e-3 * dk_scale
+    assert ((dv - do).norm() / do.norm()).item() <= 1e-2
+
+
+class _HostView:
+    """bf16 host tensor [L, H, d] that hands the oracle float32 numpy slices on
+    indexing (exact up-cast), so only the slices it touches are converted."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, idx):
+        return self.t[idx].to(torch.float32).numpy()
+
+
+def _sampled_check(w, t, out, g, rows_per_head, n_keys, seed):
+    oc, ox, lse = out
+    rng = np.random.default_rng(seed)
+    L = w.L
+    fv = {k: (_HostView(v[0].cpu()) if v is not None else None) for k, v in t.items()}
+    streams = [0, 1] if w.has_clean_queries else [1]
+    samples = []
+    for h in range(w.Hq):
+        for _ in range(rows_per_head):
+            samples.append((int(rng.choice(streams)), int(rng.integers(0, L)), h))
+    ref = O.sampled_rows(fv["q_clean"], fv["k_clean"], fv["v_clean"], fv["q_corr"], fv["k_corr"],
+                         fv["v_corr"], fv["do_clean"], fv["do_corr"], w.M, w.scale, samples)
+    o_err, z_err = 0.0, 0.0
+    dq_got, dq_want = [], []
+    for (qs, i, h), (o, z, D, dq) in ref.items():
+        og = (oc if qs == 0 else ox)[0, i, h].double().cpu().numpy()
+        o_err = max(o_err, float(np.abs(og - o).max()))
+        z_err = max(z_err, abs(lse[0, qs, h, i].item() - z))
+        dq_got.append(g["dq_clean" if qs == 0 else "dq_corr"][0, i, h].double().cpu().numpy())
+        dq_want.append(dq)
+    assert o_err <= TOL_O, o_err
+    assert z_err <= TOL_LSE, z_err
+    assert rel_fro(np.array(dq_got), np.array(dq_want)) <= TOL_REL
+    # keys: corrupted keys (read by their own block) and late clean keys
+    keys = []
+    for _ in range(n_keys):
+        g_ = int(rng.integers(0, w.Hkv))
+        keys.append((1, int(rng.integers(0, L)), g_))
+        keys.append((0, int(rng.integers(L - 2 * w.M, L - w.M)), g_))
+    kref = O.sampled_keys(fv["q_clean"], fv["k_clean"], fv["v_clean"], fv["q_corr"], fv["k_corr"],
+                          fv["v_corr"], fv["do_clean"], fv["do_corr"], w.M, w.scale, keys)
+    got_k, want_k, got_v, want_v = [], [], [], []
+    for (ks, j, gg), (dk, dv) in kref.items():
+        sfx = "clean" if ks == 0 else "corr"
+        got_k.append(g["dk_" + sfx][0, j, gg].double().cpu().numpy())
+        got_v.append(g["dv_" + sfx][0, j, gg].double().cpu().numpy())
+        want_k.append(dk)
+        want_v.append(dv)
+    assert rel_fro(np.array(got_k), np.array(want_k)) <= TOL_REL
+    assert rel_fro(np.array(got_v), np.array(want_v)) <= TOL_REL
+
+
+@pytest.mark.parametrize("name,rows,keys,seed", [("dense14b", 256, 8, 101), ("sharded", 16, 4, 102),
+                                                  ("long", 8, 4, 103), ("drafter", 2, 2, 104)])
+def test_full_size_workloads_sampled(name, rows, keys, seed):
+    w = WORKLOADS[name]
+    t, out, g = run_gpu(w)
+    _invariants(w, t, g)
+    _sampled_check(w, t, out, g, rows, keys, seed=seed)
+    del t, out, g
+    torch.cuda.empty_cache()

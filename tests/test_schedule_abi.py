@@ -1,0 +1,191 @@
+"""CPU tests of the C-ABI library: exported symbols, host scheduler bit-exact
+against the oracle's mask-derived tile set, dual-end / zigzag ownership,
+argument validation.  No kernel is launched (no GPU needed)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from block_diffusion_lm_gb300 import csbp
+from block_diffusion_lm_gb300.inputs import WORKLOADS
+from oracle import csbp_oracle as O
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from block_diffusion_lm_gb300 import build
+    build.build()
+
+
+def expand(words, info, P):
+    """Work list -> (fwd set, bwd set, fwd costs, bwd costs) of
+    (q_stream, q_tile, kv_stream, kv_tile, full, part) tuples."""
+    h = words[:16]
+    assert h[0] == 0x43534250 and h[1] == 1
+    off_ft, off_fs, off_bt, off_bs, total = (int(x) for x in h[11:16])
+    assert total == len(words)
+    fwd, bwd, fc, bc = set(), set(), [], []
+    seen = set()
+    for t in range(info.n_fwd_tasks):
+        qs, qt, part, sb, sc, cost = (int(x) for x in words[off_ft + 8 * t: off_ft + 8 * t + 6])
+        fc.append(cost)
+        n = 0
+        for s in range(sb, sb + sc):
+            ks, b, e, fl = (int(x) for x in words[off_fs + 4 * s: off_fs + 4 * s + 4])
+            for kt in range(b, e):
+                key = (qs, qt, ks, kt)
+                assert key not in seen  # every tile pair appears once
+                seen.add(key)
+                fwd.add(key + (not (fl & 1), part))
+                n += 1
+        assert n == cost
+    for t in range(info.n_bwd_tasks):
+        ks, kt, part, sb, sc, cost = (int(x) for x in words[off_bt + 8 * t: off_bt + 8 * t + 6])
+        bc.append(cost)
+        n = 0
+        for s in range(sb, sb + sc):
+            qs, b, e, fl = (int(x) for x in words[off_bs + 4 * s: off_bs + 4 * s + 4])
+            for qt in range(b, e):
+                bwd.add((qs, qt, ks, kt, not (fl & 1), part))
+                n += 1
+        assert n == cost
+    return fwd, bwd, fc, bc
+
+
+def test_library_exports_every_declared_symbol():
+    L = csbp.lib()
+    names = csbp.header_functions()
+    assert set(names) >= {"csbp_block_schedule", "csbp_attn_fwd", "csbp_attn_bwd",
+                          "csbp_lse_merge"}
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.csbp_version() >= 100
+    for code, name in csbp.STATUS.items():
+        assert L.csbp_status_string(code)
+
+
+SWEEP = [
+    # L, M, T, P, has_clean
+    (256, 16, 32, 1, True), (256, 32, 32, 1, True), (256, 64, 32, 1, True),
+    (512, 16, 64, 2, True), (512, 8, 32, 4, True), (480, 16, 32, 1, True),   # ragged tail
+    (256, 1, 32, 1, True), (256, 256, 32, 1, True), (256, 16, 32, 1, False),
+    (512, 16, 32, 2, False), (200, 8, 32, 1, True), (384, 128, 128, 1, True),
+    (1024, 64, 128, 1, True), (1024, 32, 128, 4, True), (1040, 16, 128, 1, True),
+]
+
+
+@pytest.mark.parametrize("L,M,T,P,clean", SWEEP)
+def test_schedule_matches_oracle_tile_set_bit_exactly(L, M, T, P, clean):
+    prob = csbp.make_problem(1, L, M, 2, 1, 64, P=P, has_clean_queries=clean, tile=T)
+    bo, co, words, info = csbp.block_schedule(prob)
+    fwd, bwd, fc, bc = expand(words, info, P)
+    want = O.tile_pairs(L, M, T, T, P, clean)
+    if P == 1:
+        got_fwd = {x[:5] + ((1 if x[2] == 1 else 0),) for x in fwd}
+        assert all(x[5] == -1 for x in fwd)
+    else:
+        got_fwd = fwd
+    assert got_fwd == want
+    got_bwd = {x for x in bwd}
+    if P == 1:
+        got_bwd = {x[:5] + ((1 if x[2] == 1 else 0),) for x in bwd}
+    assert got_bwd == want
+    assert info.tile_pairs == len(want)
+    # heaviest first
+    assert fc == sorted(fc, reverse=True)
+    assert bc == sorted(bc, reverse=True)
+    # every key tile of both copies has exactly one backward task
+    nT = -(-L // T)
+    assert info.n_bwd_tasks == 2 * nT
+
+
+@pytest.mark.parametrize("L,M,P", [(64, 4, 2), (128, 4, 4), (96, 4, 3), (4096, 32, 8)])
+def test_ownership_matches_oracle(L, M, P):
+    prob = csbp.make_problem(1, L, M, 1, 1, 64, P=P, tile=16 if L < 4096 else 128)
+    if (L // (2 * P)) % prob.tile_kv:
+        prob.tile_q = prob.tile_kv = 4
+    bo, co, _, _ = csbp.block_schedule(prob)
+    np.testing.assert_array_equal(bo, O.block_owner(L, M, P))
+    np.testing.assert_array_equal(co, O.chunk_owner(L, P))
+
+
+@pytest.mark.parametrize("name", ["tiny", "dense14b", "sharded", "long"])
+def test_full_size_schedules_closed_form(name):
+    """Tile-pair count nT(nT+1)+nT at the workload sizes (M < 128), and equal
+    tile counts per clean shard under the zigzag pairing."""
+    w = WORKLOADS[name]
+    prob = csbp.make_problem(w.batch, w.L, w.M, w.Hq, w.Hkv, w.d, P=w.P,
+                             has_clean_queries=w.has_clean_queries)
+    _, _, words, info = csbp.block_schedule(prob)
+    nT = w.L // 128
+    assert info.tile_pairs == nT * (nT + 1) + nT
+    if w.P > 1:
+        fwd, _, _, _ = expand(words, info, w.P)
+        per = np.zeros(w.P + 1, np.int64)
+        for x in fwd:
+            per[x[5]] += 1
+        assert np.all(per[:w.P] == per[0])
+        assert per[w.P] == nT
+
+
+def test_drafter_schedule_count():
+    """Corrupted queries only, L = 2^20, M = 16: nT(nT+1)/2 + nT tile pairs
+    (clean tiles 0..t plus the own corrupted tile per query tile)."""
+    w = WORKLOADS["drafter"]
+    prob = csbp.make_problem(1, w.L, w.M, w.Hq, w.Hkv, w.d, has_clean_queries=False)
+    info = csbp.ScheduleInfo()
+    st = csbp.lib().csbp_block_schedule(ctypes.byref(prob), None, None, None, 0,
+                                        ctypes.byref(info))
+    assert st == -6  # capacity query
+    nT = w.L // 128
+    assert info.tile_pairs == nT * (nT + 1) // 2 + nT
+    assert info.n_bwd_tasks == 2 * nT
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("M", 3, -1),            # L % M != 0
+    ("Hkv", 3, -1),          # Hq % Hkv != 0
+    ("d", 96, -2),           # unsupported head dim
+    ("P", 3, -2),            # B % 2P != 0
+    ("scale", 0.0, -1),
+    ("L", 0, -1),
+    ("has_clean_queries", 2, -1),
+])
+def test_schedule_rejects_invalid_problems(field, value, code):
+    prob = csbp.make_problem(1, 1024, 64, 4, 2, 64)
+    setattr(prob, field, value)
+    info = csbp.ScheduleInfo()
+    st = csbp.lib().csbp_block_schedule(ctypes.byref(prob), None, None, None, 0, ctypes.byref(info))
+    assert st == code
+
+
+def test_workspace_sizes():
+    prob = csbp.make_problem(2, 1024, 64, 4, 2, 128, P=4)
+    rows = 2 * 1024
+    fwd = csbp.workspace_bytes(prob, 0)
+    bwd = csbp.workspace_bytes(prob, 1)
+    assert fwd >= 256 + 5 * 2 * rows * 4 * 128 * 4 + 5 * 2 * rows * 4 * 4
+    assert bwd >= 256 + 2 * rows * 4 * 4 + 2 * rows * 4 * 128 * 4
+    prob.d = 96
+    assert csbp.workspace_bytes(prob, 0) == 0
+
+
+def test_entry_points_reject_bad_arguments_without_launching():
+    """Null pointers and misalignment are refused before anything is enqueued
+    (no CUDA call is made on these paths, so this runs without a GPU)."""
+    L = csbp.lib()
+    prob = csbp.make_problem(1, 1024, 64, 2, 2, 64)
+    info = csbp.ScheduleInfo()
+    inp = csbp.Inputs()
+    assert L.csbp_attn_fwd(ctypes.byref(prob), ctypes.byref(inp), None, ctypes.byref(info),
+                           None, None, None, None, 0, None) == -1
+    assert L.csbp_attn_bwd(ctypes.byref(prob), None, None, ctypes.byref(info), *([None] * 12),
+                           0, None) == -1
+    arr = (ctypes.c_void_p * 1)(None)
+    assert L.csbp_lse_merge(0, arr, arr, 16, 2, 64, None, None, None) == -1
+    assert L.csbp_lse_merge(1, arr, arr, 16, 2, 64, None, None, None) == -1
+    # misaligned (odd) pointers
+    bad = ctypes.c_void_p(0x1001)
+    inp = csbp.Inputs(bad, bad, bad, bad, bad, bad)
+    assert L.csbp_attn_fwd(ctypes.byref(prob), ctypes.byref(inp), bad, ctypes.byref(info),
+                           bad, bad, bad, bad, 1 << 20, None) == -1
