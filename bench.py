@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--impl", default="csbp", choices=["csbp", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--L", type=int, default=None,
+                    help="override the sequence length (profiling captures of a smaller case)")
     return ap.parse_args()
 
 
@@ -178,8 +180,12 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
+    import dataclasses
+
     from block_diffusion_lm_gb300.inputs import WORKLOADS
     w = WORKLOADS[args.config]
+    if args.L is not None:
+        w = dataclasses.replace(w, name=f"{w.name}@L={args.L}", L=args.L)
     flops = w.useful_fwd_flops() + w.useful_bwd_flops()
     config = {"workload": w.name, "batch": w.batch, "L": w.L, "M": w.M, "Hq": w.Hq,
               "Hkv": w.Hkv, "d": w.d, "P": w.P, "clean_queries": w.has_clean_queries,

@@ -9,18 +9,25 @@
 // with the block owner, clean dK/dV are summed for the clean-shard owner).
 //
 // One CTA owns one 128-row key tile of one (batch, KV head) and walks every
-// (query head of the GQA group, query tile) its work-list task lists, so dK/dV
-// accumulate in TMEM for the whole group and are written once.  Roles:
-//   warp 0 lane 0  TMA producer: K, V once; Q (2 stages) and dO per step
-//   warp 1 lane 0  MMA issuer:   S^T = K Q^T, dP^T = V dO^T; dV += P^T dO;
-//                                dK += dS^T Q; dQ_tile = dS K
-//   warps 4..7     thread t owns key row t for S^T/dP^T/dV/dK and query row
-//                  t for the dQ tile; P^T and then dS^T go through one
-//                  128B-swizzled shared tile that serves as K-major A operand
-//                  (dV, dK) and, read transposed, as MN-major A operand (dQ).
-//                  dQ tiles are added into an fp32 accumulator with vector
-//                  atomics.
-// TMEM columns: S^T (later the dQ tile) at 0, dP^T at 128, dV at 256, dK at 384.
+// (query head of the GQA group, 128-row query tile) its work-list task lists,
+// so dK/dV accumulate in TMEM for the whole group and are written once.  Each
+// query tile is processed as two 64-row sub-tiles by two compute warpgroups
+// that alternate, so the tensor core works on one sub-tile while the other
+// warpgroup computes exponentials.  Roles (384 threads):
+//   warp 0 lane 0  TMA producer: K, V once; per sub-tile Q (4 stages) with its
+//                  LSE and D slices, and dO (3 stages)
+//   warp 1 lane 0  MMA issuer, per sub-tile s (stream w = s & 1):
+//                    dV += P_s^T dO_s;  dK += dS_s^T Q_s;  dQ_s^T = K^T dS_s^T
+//                    then dP^T_{s+1} = V dO_{s+1}^T and S^T_{s+2} = K Q_{s+2}^T
+//   warps 4..7 / 8..11  compute streams 0 / 1: thread t owns key row t (TMEM
+//                  lane t); builds P^T and dS^T (fp32 math, bf16 operands)
+//                  through the stream's 128B-swizzled shared tile, then copies
+//                  dQ^T (thread t = head-dim row t) out of TMEM and adds it to
+//                  the fp32 dQ accumulator: one warp-wide atomic add covers 32
+//                  consecutive head-dim elements (128 contiguous bytes).
+// TMEM columns: stream w has S^T at 128w and dP^T (then dQ^T) at 128w + 64;
+// dV at 256, dK at 256 + d.  For d = 64 the dQ^T MMA runs with M = 128 and
+// the upper 64 rows of K^T read a zero tile.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -31,47 +38,56 @@ namespace csbp {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kSub = 64;          // query rows per sub-tile
+constexpr int kQStages = 4;
+constexpr int kDOStages = 3;
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdLayout {
-  static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kBoxBytes = kTile * 64 * 2;
-  static constexpr int kXBytes = kTile * kTile * 2;
+  static constexpr int kKVBytes = kTile * D * 2;     // K or V tile
+  static constexpr int kKVBox = kTile * 128;         // one 64-column box of K/V
+  static constexpr int kSubBytes = kSub * D * 2;     // Q or dO sub-tile
+  static constexpr int kSubBox = kSub * 128;         // one 64-column box of a sub-tile
+  static constexpr int kXBytes = kTile * kSub * 2;   // P^T / dS^T of one stream
+  static constexpr int kStatBytes = 2 * kSub * 4;    // LSE and D of one sub-tile
   static constexpr int kK = 0;
-  static constexpr int kV = kK + kTileBytes;
-  static constexpr int kQ = kV + kTileBytes;        // 2 stages
-  static constexpr int kDO = kQ + 2 * kTileBytes;   // 1 stage
-  static constexpr int kX = kDO + kTileBytes;       // P^T, then dS^T
-  static constexpr int kStat = kX + kXBytes;        // [4 warps][lse2 | D][128] fp32
-  static constexpr int kBytes = kStat + 4 * 2 * kTile * 4;
+  static constexpr int kV = kK + kKVBytes;
+  static constexpr int kZero = kV + kKVBytes;        // zero K^T rows (d = 64 only)
+  static constexpr int kQ = kZero + (D == 64 ? kKVBox : 0);
+  static constexpr int kDO = kQ + kQStages * kSubBytes;
+  static constexpr int kX = kDO + kDOStages * kSubBytes;
+  static constexpr int kStat = kX + 2 * kXBytes;
+  static constexpr int kBytes = kStat + kQStages * kStatBytes;
   static constexpr int kDynSmem = kBytes + 1024;
   static constexpr uint32_t kColDV = 256;
-  static constexpr uint32_t kColDK = 256 + (D > 64 ? 128 : 64);
+  static constexpr uint32_t kColDK = 256 + D;
 };
 
 enum BwdBar {
   C_KV_FULL = 0,
-  C_Q_FULL,  // [2]
-  C_Q_EMPTY = C_Q_FULL + 2,
-  C_DO_FULL = C_Q_EMPTY + 2,
-  C_DO_EMPTY,
-  C_S_FULL,
-  C_P_READY,
-  C_X_FREE,
-  C_DS_READY,
-  C_X_FREE2,
-  C_DQ_FULL,
-  C_DQ_FREE,
-  C_ACC_DONE,
+  C_Q_FULL,                          // [kQStages]
+  C_Q_EMPTY = C_Q_FULL + kQStages,   // [kQStages]
+  C_DO_FULL = C_Q_EMPTY + kQStages,  // [kDOStages]
+  C_DO_EMPTY = C_DO_FULL + kDOStages,
+  C_S_FULL = C_DO_EMPTY + kDOStages,  // per stream [2]
+  C_DP_FULL = C_S_FULL + 2,
+  C_P_READY = C_DP_FULL + 2,
+  C_X_FREE = C_P_READY + 2,
+  C_DS_READY = C_X_FREE + 2,
+  C_X_FREE2 = C_DS_READY + 2,
+  C_DQ_FULL = C_X_FREE2 + 2,
+  C_DQ_FREE = C_DQ_FULL + 2,
+  C_ACC_DONE = C_DQ_FREE + 2,
   C_DRAIN,
   C_COUNT
 };
 
-// Walk over (query head in group, segment, query tile) of a backward task.
+// Walk over (query head in group, segment, 128-row query tile) of a task.
 struct QWalk {
   const int32_t* seg0;
-  int n_segs, g, G, si, t, end, stream, flags;
+  int n_segs, g, si, t, end, stream, flags;
   __device__ void load_seg() {
     const int32_t* s = seg0 + si * kSegWords;
     stream = s[0];
@@ -79,10 +95,9 @@ struct QWalk {
     end = s[2];
     flags = s[3];
   }
-  __device__ void start(const int32_t* s, int n, int groups) {
+  __device__ void start(const int32_t* s, int n) {
     seg0 = s;
     n_segs = n;
-    G = groups;
     g = 0;
     si = 0;
     if (n > 0) load_seg();
@@ -97,9 +112,36 @@ struct QWalk {
   }
 };
 
-__device__ __forceinline__ bool mask_allows(int q_stream, int k_stream, int qb, int kb) {
-  if (q_stream == 0) return k_stream == 0 && kb <= qb;
-  return k_stream == 0 ? (kb < qb) : (kb == qb);
+// Query positions [lo, hi) that may read key block kb of copy k_stream, for
+// queries of copy q_stream: clean keys are read by clean queries of the same
+// or later blocks and by corrupted queries of later blocks; corrupted keys
+// only by corrupted queries of their own block.
+__device__ __forceinline__ void allowed_query_range(int q_stream, int k_stream, int kb, int M,
+                                                    int L, bool k_valid, int& lo, int& hi) {
+  if (!k_valid || (q_stream == 0 && k_stream == 1)) {
+    lo = hi = 0;
+    return;
+  }
+  if (k_stream == 0) {
+    lo = (q_stream == 0) ? kb * M : (kb + 1) * M;
+    hi = L;
+  } else {
+    lo = kb * M;
+    hi = min((kb + 1) * M, L);
+  }
+}
+
+// S^T (or dP^T) of one sub-tile: M = 128 key rows, N = 64 query rows, K = d.
+template <int D>
+__device__ __forceinline__ void issue_kq(uint32_t d_tmem, uint32_t a_kv, uint32_t b_sub) {
+  using Lay = BwdLayout<D>;
+  constexpr uint32_t idesc = idesc_bf16_f32(128, kSub, false, false);
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    umma_bf16_ss(d_tmem, sdesc_sw128(a_kv + (k >> 2) * Lay::kKVBox + (k & 3) * 32, 16, 1024),
+                 sdesc_sw128(b_sub + (k >> 2) * Lay::kSubBox + (k & 3) * 32, 16, 1024), idesc,
+                 k > 0 ? 1u : 0u);
+  }
 }
 
 template <int D>
@@ -108,7 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap tm_k0, const __grid_constant__ CUtensorMap tm_k1,
                const __grid_constant__ CUtensorMap tm_v0, const __grid_constant__ CUtensorMap tm_v1,
                const __grid_constant__ CUtensorMap tm_do0,
-               const __grid_constant__ CUtensorMap tm_do1, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_do1,
+               const __grid_constant__ CUtensorMap tm_lse,
+               const __grid_constant__ CUtensorMap tm_dsum, const BwdParams p) {
   using Lay = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -130,15 +174,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int k_tile = tw[1];
   const int32_t* segs = p.segs + static_cast<int64_t>(tw[3]) * kSegWords;
   const int n_segs = tw[4];
-  const int n_iters = tw[5] * p.G;
+  const int n_sub = 2 * tw[5] * p.G;  // two 64-row sub-tiles per query tile
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C_COUNT; ++i) {
-      const bool per_warp = (i == C_P_READY || i == C_DS_READY || i == C_DQ_FREE);
+      const bool per_warp = (i >= C_P_READY && i < C_P_READY + 2) ||
+                            (i >= C_DS_READY && i < C_DS_READY + 2) ||
+                            (i >= C_DQ_FREE && i < C_DQ_FREE + 2);
       mbar_init(&bars[i], per_warp ? 4 : 1);
     }
     abort_flag = 0;
     fence_mbarrier_init();
+  }
+  if (D == 64) {  // zero rows of K^T for the padded dQ^T MMA
+    uint4* z = reinterpret_cast<uint4*>(smem + Lay::kZero);
+    for (int i = threadIdx.x; i < Lay::kKVBox / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, 512);
@@ -155,255 +206,289 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sDO = smem_u32(smem + Lay::kDO);
   const uint32_t sX = smem_u32(smem + Lay::kX);
 
-  if (n_iters > 0 && warp == 0 && lane == 0) {
+  if (n_sub > 0 && warp == 0 && lane == 0) {
     // ===================== TMA producer
     const void* tk = k_stream ? static_cast<const void*>(&tm_k1) : static_cast<const void*>(&tm_k0);
     const void* tv = k_stream ? static_cast<const void*>(&tm_v1) : static_cast<const void*>(&tm_v0);
-    mbar_arrive_expect_tx(&bars[C_KV_FULL], 2 * Lay::kTileBytes);
+    mbar_arrive_expect_tx(&bars[C_KV_FULL], 2 * Lay::kKVBytes);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
-      tma_load_3d(smem + Lay::kK + c * Lay::kBoxBytes, tk, &bars[C_KV_FULL], kvh * D + c * 64,
+      tma_load_3d(smem + Lay::kK + c * Lay::kKVBox, tk, &bars[C_KV_FULL], kvh * D + c * 64,
                   k_tile * kTile, bz);
-      tma_load_3d(smem + Lay::kV + c * Lay::kBoxBytes, tv, &bars[C_KV_FULL], kvh * D + c * 64,
+      tma_load_3d(smem + Lay::kV + c * Lay::kKVBox, tv, &bars[C_KV_FULL], kvh * D + c * 64,
                   k_tile * kTile, bz);
     }
     QWalk w;
-    w.start(segs, n_segs, p.G);
+    w.start(segs, n_segs);
     int nq = 0, ndo = 0;
     bool ok = true;
-    for (int i = 0; i < n_iters; ++i, w.next()) {
-      const int st = i & 1;
+    for (int s = 0; s < n_sub && ok; ++s) {
       const int h = kvh * p.G + w.g;
-      const void* tq = w.stream ? static_cast<const void*>(&tm_q1) : static_cast<const void*>(&tm_q0);
-      const void* td = w.stream ? static_cast<const void*>(&tm_do1) : static_cast<const void*>(&tm_do0);
-      if (i >= 2) ok = mbar_wait(&bars[C_Q_EMPTY + st], ((i - 2) >> 1) & 1, p.status, &abort_flag);
+      const int qs = w.stream;
+      const int q0 = w.t * kTile + (s & 1) * kSub;
+      const void* tq = qs ? static_cast<const void*>(&tm_q1) : static_cast<const void*>(&tm_q0);
+      const void* td = qs ? static_cast<const void*>(&tm_do1) : static_cast<const void*>(&tm_do0);
+      const int qst = s % kQStages;
+      if (s >= kQStages)
+        ok = mbar_wait(&bars[C_Q_EMPTY + qst], ((s / kQStages) - 1) & 1, p.status, &abort_flag);
       if (!ok) break;
-      mbar_arrive_expect_tx(&bars[C_Q_FULL + st], Lay::kTileBytes);
+      mbar_arrive_expect_tx(&bars[C_Q_FULL + qst], Lay::kSubBytes + Lay::kStatBytes);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(smem + Lay::kQ + st * Lay::kTileBytes + c * Lay::kBoxBytes, tq,
-                    &bars[C_Q_FULL + st], h * D + c * 64, w.t * kTile, bz);
-      nq = i + 1;
-      if (i >= 1) ok = mbar_wait(&bars[C_DO_EMPTY], (i - 1) & 1, p.status, &abort_flag);
+        tma_load_3d(smem + Lay::kQ + qst * Lay::kSubBytes + c * Lay::kSubBox, tq,
+                    &bars[C_Q_FULL + qst], h * D + c * 64, q0, bz);
+      uint8_t* stat = smem + Lay::kStat + qst * Lay::kStatBytes;
+      tma_load_2d(stat, &tm_lse, &bars[C_Q_FULL + qst], q0, (bz * 2 + qs) * p.Hq + h);
+      tma_load_2d(stat + kSub * 4, &tm_dsum, &bars[C_Q_FULL + qst], q0,
+                  (qs * p.batch + bz) * p.Hq + h);
+      nq = s + 1;
+      const int dst = s % kDOStages;
+      if (s >= kDOStages)
+        ok = mbar_wait(&bars[C_DO_EMPTY + dst], ((s / kDOStages) - 1) & 1, p.status, &abort_flag);
       if (!ok) break;
-      mbar_arrive_expect_tx(&bars[C_DO_FULL], Lay::kTileBytes);
+      mbar_arrive_expect_tx(&bars[C_DO_FULL + dst], Lay::kSubBytes);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(smem + Lay::kDO + c * Lay::kBoxBytes, td, &bars[C_DO_FULL], h * D + c * 64,
-                    w.t * kTile, bz);
-      ndo = i + 1;
+        tma_load_3d(smem + Lay::kDO + dst * Lay::kSubBytes + c * Lay::kSubBox, td,
+                    &bars[C_DO_FULL + dst], h * D + c * 64, q0, bz);
+      ndo = s + 1;
+      if (s & 1) w.next();
     }
     if (!ok) {
+      // drain the loads that may still be in flight
       mbar_wait(&bars[C_KV_FULL], 0, nullptr, nullptr, 200000000ull);
-      for (int i = (nq > 2 ? nq - 2 : 0); i < nq; ++i)
-        mbar_wait(&bars[C_Q_FULL + (i & 1)], (i >> 1) & 1, nullptr, nullptr, 200000000ull);
-      if (ndo > 0) mbar_wait(&bars[C_DO_FULL], (ndo - 1) & 1, nullptr, nullptr, 200000000ull);
+      for (int s = (nq > kQStages ? nq - kQStages : 0); s < nq; ++s)
+        mbar_wait(&bars[C_Q_FULL + s % kQStages], (s / kQStages) & 1, nullptr, nullptr, 200000000ull);
+      for (int s = (ndo > kDOStages ? ndo - kDOStages : 0); s < ndo; ++s)
+        mbar_wait(&bars[C_DO_FULL + s % kDOStages], (s / kDOStages) & 1, nullptr, nullptr,
+                  200000000ull);
     }
-  } else if (n_iters > 0 && warp == 1 && lane == 0) {
+  } else if (n_sub > 0 && warp == 1 && lane == 0) {
     // ===================== MMA issuer
-    constexpr uint32_t idesc_sq = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-    constexpr uint32_t idesc_kd = idesc_bf16_f32(128, D, false, true);     // dV, dK
-    constexpr uint32_t idesc_q = idesc_bf16_f32(128, D, true, true);       // dQ
-    bool ok = mbar_wait(&bars[C_KV_FULL], 0, p.status, &abort_flag);
-    for (int i = 0; i < n_iters && ok; ++i) {
-      const int st = i & 1;
-      const uint32_t q_s = sQ + st * Lay::kTileBytes;
-      ok = mbar_wait(&bars[C_Q_FULL + st], (i >> 1) & 1, p.status, &abort_flag) &&
-           mbar_wait(&bars[C_DO_FULL], i & 1, p.status, &abort_flag) &&
-           (i == 0 || mbar_wait(&bars[C_DQ_FREE], (i - 1) & 1, p.status, &abort_flag));
-      if (!ok) break;
+    constexpr uint32_t idesc_kd = idesc_bf16_f32(128, D, false, true);  // dV, dK
+    constexpr uint32_t idesc_q = idesc_bf16_f32(128, kSub, true, true);  // dQ^T
+    auto qbuf = [&](int s) { return sQ + (s % kQStages) * Lay::kSubBytes; };
+    auto dobuf = [&](int s) { return sDO + (s % kDOStages) * Lay::kSubBytes; };
+    auto wait_q = [&](int s) {
+      return mbar_wait(&bars[C_Q_FULL + s % kQStages], (s / kQStages) & 1, p.status, &abort_flag);
+    };
+    auto wait_do = [&](int s) {
+      return mbar_wait(&bars[C_DO_FULL + s % kDOStages], (s / kDOStages) & 1, p.status, &abort_flag);
+    };
+    bool ok = mbar_wait(&bars[C_KV_FULL], 0, p.status, &abort_flag) && wait_q(0) && wait_do(0);
+    if (ok) {
+      tc_fence_after_sync();
+      issue_kq<D>(tmem + 0, sK, qbuf(0));
+      umma_commit(&bars[C_S_FULL + 0]);
+      issue_kq<D>(tmem + 64, sV, dobuf(0));
+      umma_commit(&bars[C_DP_FULL + 0]);
+      if (n_sub > 1) {
+        ok = wait_q(1);
+        if (ok) {
+          tc_fence_after_sync();
+          issue_kq<D>(tmem + 128, sK, qbuf(1));
+          umma_commit(&bars[C_S_FULL + 1]);
+        }
+      }
+    }
+    for (int s = 0; s < n_sub && ok; ++s) {
+      const int w = s & 1;
+      const int k = s >> 1;
+      const uint32_t xw = sX + w * Lay::kXBytes;
+      // ---- finish sub-tile s
+      if (!mbar_wait(&bars[C_P_READY + w], k & 1, p.status, &abort_flag)) break;
       tc_fence_after_sync();
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k >> 2) * Lay::kBoxBytes + (k & 3) * 32;
-        umma_bf16_ss(tmem + 0, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(q_s + off, 16, 1024),
-                     idesc_sq, k > 0 ? 1u : 0u);
-      }
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k >> 2) * Lay::kBoxBytes + (k & 3) * 32;
-        umma_bf16_ss(tmem + 128, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024),
-                     idesc_sq, k > 0 ? 1u : 0u);
-      }
-      umma_commit(&bars[C_S_FULL]);
-      if (!mbar_wait(&bars[C_P_READY], i & 1, p.status, &abort_flag)) break;
+      for (int kk = 0; kk < kSub / 16; ++kk)
+        umma_bf16_ss(tmem + Lay::kColDV, sdesc_sw128(xw + kk * 32, 16, 1024),
+                     sdesc_sw128(dobuf(s) + kk * 2048, Lay::kSubBox, 1024), idesc_kd,
+                     (s > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&bars[C_X_FREE + w]);
+      umma_commit(&bars[C_DO_EMPTY + s % kDOStages]);
+      if (!mbar_wait(&bars[C_DS_READY + w], k & 1, p.status, &abort_flag)) break;
       tc_fence_after_sync();
 #pragma unroll
-      for (int k = 0; k < kTile / 16; ++k) {
-        const uint64_t ad = sdesc_sw128(sX + (k >> 2) * Lay::kBoxBytes + (k & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(sDO + k * 2048, Lay::kBoxBytes, 1024);
-        umma_bf16_ss(tmem + Lay::kColDV, ad, bd, idesc_kd, (i > 0 || k > 0) ? 1u : 0u);
-      }
-      umma_commit(&bars[C_X_FREE]);
-      umma_commit(&bars[C_DO_EMPTY]);
-      if (!mbar_wait(&bars[C_DS_READY], i & 1, p.status, &abort_flag)) break;
-      tc_fence_after_sync();
+      for (int kk = 0; kk < kSub / 16; ++kk)
+        umma_bf16_ss(tmem + Lay::kColDK, sdesc_sw128(xw + kk * 32, 16, 1024),
+                     sdesc_sw128(qbuf(s) + kk * 2048, Lay::kSubBox, 1024), idesc_kd,
+                     (s > 0 || kk > 0) ? 1u : 0u);
+      // dQ^T = K^T dS^T: A = K tile read MN-major (M = d), B = dS^T (N = 64 queries)
+      const uint32_t a_lbo = (D == 64) ? static_cast<uint32_t>(Lay::kZero - Lay::kK) : Lay::kKVBox;
 #pragma unroll
-      for (int k = 0; k < kTile / 16; ++k) {
-        const uint64_t ad = sdesc_sw128(sX + (k >> 2) * Lay::kBoxBytes + (k & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(q_s + k * 2048, Lay::kBoxBytes, 1024);
-        umma_bf16_ss(tmem + Lay::kColDK, ad, bd, idesc_kd, (i > 0 || k > 0) ? 1u : 0u);
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        umma_bf16_ss(tmem + w * 128 + 64, sdesc_sw128(sK + kk * 2048, a_lbo, 1024),
+                     sdesc_sw128(xw + kk * 2048, Lay::kXBytes, 1024), idesc_q, kk > 0 ? 1u : 0u);
+      umma_commit(&bars[C_DQ_FULL + w]);
+      umma_commit(&bars[C_Q_EMPTY + s % kQStages]);
+      umma_commit(&bars[C_X_FREE2 + w]);
+      // ---- dP^T of sub-tile s+1 (other stream; its columns held dQ^T_{s-1})
+      if (s + 1 < n_sub) {
+        const int w1 = w ^ 1;
+        if ((s >= 1 && !mbar_wait(&bars[C_DQ_FREE + w1], ((s - 1) >> 1) & 1, p.status, &abort_flag)) ||
+            !wait_do(s + 1))
+          break;
+        tc_fence_after_sync();
+        issue_kq<D>(tmem + w1 * 128 + 64, sV, dobuf(s + 1));
+        umma_commit(&bars[C_DP_FULL + w1]);
       }
-#pragma unroll
-      for (int k = 0; k < kTile / 16; ++k) {
-        const uint64_t ad = sdesc_sw128(sX + k * 2048, Lay::kBoxBytes, 1024);
-        const uint64_t bd = sdesc_sw128(sK + k * 2048, Lay::kBoxBytes, 1024);
-        umma_bf16_ss(tmem + 0, ad, bd, idesc_q, k > 0 ? 1u : 0u);
+      // ---- S^T of sub-tile s+2 (this stream; read before P_READY_s)
+      if (s + 2 < n_sub) {
+        if (!wait_q(s + 2)) break;
+        tc_fence_after_sync();
+        issue_kq<D>(tmem + w * 128, sK, qbuf(s + 2));
+        umma_commit(&bars[C_S_FULL + w]);
       }
-      umma_commit(&bars[C_DQ_FULL]);
-      umma_commit(&bars[C_Q_EMPTY + st]);
-      umma_commit(&bars[C_X_FREE2]);
     }
     umma_commit(&bars[C_ACC_DONE]);
     umma_commit(&bars[C_DRAIN]);
     mbar_wait(&bars[C_DRAIN], 0, nullptr, nullptr, 500000000ull);
   } else if (warp >= 4) {
-    // ===================== compute warpgroup
-    const int r = threadIdx.x - 128;
-    const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    // ===================== compute streams
+    const int w = (warp >= 8) ? 1 : 0;
+    const int r = threadIdx.x - 128 * (w + 1);  // key row (TMEM lane)
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t colS = w * 128, colDP = w * 128 + 64;
     const int kpos = k_tile * kTile + r;
     const bool k_valid = kpos < p.L;
     const int kb = k_valid ? kpos / p.M : -1;
     const float sl2 = p.scale_log2;
-    float* stat = reinterpret_cast<float*>(smem + Lay::kStat);
-    uint8_t* xbase = smem + Lay::kX;
+    uint8_t* xbase = smem + Lay::kX + w * Lay::kXBytes;
     const bool k_ragged = (k_tile + 1) * kTile > p.L;
-    QWalk w;
-    w.start(segs, n_segs, p.G);
+    QWalk wk;
+    wk.start(segs, n_segs);
     bool ok = true;
-    for (int i = 0; i < n_iters; ++i, w.next()) {
-      const int h = kvh * p.G + w.g;
-      const int qs = w.stream;
-      const int q0 = w.t * kTile;
-      // stage LSE (log2 units) and D of the 128 query columns in this warp's
-      // own slice (warp-local sync only)
-      float* lse2 = stat + (warp - 4) * 2 * kTile;
-      float* Dq = lse2 + kTile;
-      {
-        const int64_t rbase = ((static_cast<int64_t>(bz) * 2 + qs) * p.Hq + h) * p.L;
-        const int64_t dbase = ((static_cast<int64_t>(qs) * p.batch + bz) * p.Hq + h) * p.L;
-        __syncwarp();
-#pragma unroll
-        for (int e = 0; e < kTile / 32; ++e) {
-          const int c = e * 32 + lane;
-          const int qpos = q0 + c;
-          lse2[c] = (qpos < p.L) ? p.lse[rbase + qpos] * 1.4426950408889634f : INFINITY;
-          Dq[c] = (qpos < p.L) ? p.Dsum[dbase + qpos] : 0.f;
-        }
-        __syncwarp();
+    for (int s = w; s < n_sub; s += 2, wk.next()) {
+      const int k = s >> 1;
+      const int qs = wk.stream;
+      const int h = kvh * p.G + wk.g;
+      const int q0 = wk.t * kTile + w * kSub;
+      const int qst = s % kQStages;
+      if (!mbar_wait_warp(&bars[C_S_FULL + w], k & 1, p.status, &abort_flag) ||
+          !mbar_wait_warp(&bars[C_Q_FULL + qst], (s / kQStages) & 1, p.status, &abort_flag) ||
+          (k > 0 && !mbar_wait_warp(&bars[C_X_FREE2 + w], (k - 1) & 1, p.status, &abort_flag))) {
+        ok = false;
+        break;
       }
-      if (!mbar_wait_warp(&bars[C_S_FULL], i & 1, p.status, &abort_flag)) { ok = false; break; }
-      if (i > 0 && !mbar_wait_warp(&bars[C_X_FREE2], (i - 1) & 1, p.status, &abort_flag)) { ok = false; break; }
       tc_fence_after_sync();
-      const bool masked = (w.flags & 1) || k_ragged || (q0 + kTile > p.L);
-      uint32_t ds_pack[kTile / 2];
-      int qb = q0 / p.M;
-      int qr = q0 - qb * p.M;
+      const float* lse = reinterpret_cast<const float*>(smem + Lay::kStat + qst * Lay::kStatBytes);
+      const float* Dq = lse + kSub;
+      const bool masked = (wk.flags & 1) || k_ragged || (q0 + kSub > p.L);
+      // ---- P^T = exp(S^T scale - LSE)
+      float pr[kSub];
+      tmem_ld32x2(tmem + lane_base + colS, tmem + lane_base + colS + 32, pr, pr + 32);
+      if (masked) {
+        // allowed query positions of this key row form one range [lo, hi)
+        int lo, hi;
+        allowed_query_range(qs, k_stream, kb, p.M, p.L, k_valid, lo, hi);
+        lo -= q0;
+        hi -= q0;
 #pragma unroll
-      for (int ch = 0; ch < kTile / 32; ++ch) {
-        float sv[32], dp[32];
-        tmem_ld32(tmem + lane_base + 0 + ch * 32, sv);
-        tmem_ld32(tmem + lane_base + 128 + ch * 32, dp);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int c = ch * 32 + e;
-          float pv = ex2_approx(sv[e] * sl2 - lse2[c]);
-          if (masked) {
-            const bool allow = k_valid && (q0 + c < p.L) && mask_allows(qs, k_stream, qb, kb);
-            pv = allow ? pv : 0.f;
-            if (++qr == p.M) {
-              qr = 0;
-              ++qb;
-            }
-          }
-          sv[e] = pv;
-          dp[e] = pv * (dp[e] - Dq[c]);
+        for (int c = 0; c < kSub; ++c) {
+          const float pv = ex2_approx(fmaf(pr[c], sl2, -lse[c] * kLog2e));
+          pr[c] = (c >= lo && c < hi) ? pv : 0.f;
         }
+      } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int chunk = ch * 4 + k;  // 16-byte chunk of the 256-byte row
-          uint4 v;
-          v.x = pack_bf16x2(sv[k * 8 + 0], sv[k * 8 + 1]);
-          v.y = pack_bf16x2(sv[k * 8 + 2], sv[k * 8 + 3]);
-          v.z = pack_bf16x2(sv[k * 8 + 4], sv[k * 8 + 5]);
-          v.w = pack_bf16x2(sv[k * 8 + 6], sv[k * 8 + 7]);
-          *reinterpret_cast<uint4*>(xbase + (chunk >> 3) * Lay::kBoxBytes + sw128_offset(r, chunk & 7)) = v;
-          ds_pack[chunk * 4 + 0] = pack_bf16x2(dp[k * 8 + 0], dp[k * 8 + 1]);
-          ds_pack[chunk * 4 + 1] = pack_bf16x2(dp[k * 8 + 2], dp[k * 8 + 3]);
-          ds_pack[chunk * 4 + 2] = pack_bf16x2(dp[k * 8 + 4], dp[k * 8 + 5]);
-          ds_pack[chunk * 4 + 3] = pack_bf16x2(dp[k * 8 + 6], dp[k * 8 + 7]);
-        }
+        for (int c = 0; c < kSub; ++c) pr[c] = ex2_approx(fmaf(pr[c], sl2, -lse[c] * kLog2e));
+      }
+#pragma unroll
+      for (int chunk = 0; chunk < kSub / 8; ++chunk) {
+        uint4 v;
+        v.x = pack_bf16x2(pr[chunk * 8 + 0], pr[chunk * 8 + 1]);
+        v.y = pack_bf16x2(pr[chunk * 8 + 2], pr[chunk * 8 + 3]);
+        v.z = pack_bf16x2(pr[chunk * 8 + 4], pr[chunk * 8 + 5]);
+        v.w = pack_bf16x2(pr[chunk * 8 + 6], pr[chunk * 8 + 7]);
+        *reinterpret_cast<uint4*>(xbase + sw128_offset(r, chunk)) = v;
       }
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[C_P_READY]);
-      if (!mbar_wait_warp(&bars[C_X_FREE], i & 1, p.status, &abort_flag)) { ok = false; break; }
-#pragma unroll
-      for (int chunk = 0; chunk < kTile / 8; ++chunk) {
-        uint4 v = make_uint4(ds_pack[chunk * 4 + 0], ds_pack[chunk * 4 + 1], ds_pack[chunk * 4 + 2],
-                             ds_pack[chunk * 4 + 3]);
-        *reinterpret_cast<uint4*>(xbase + (chunk >> 3) * Lay::kBoxBytes + sw128_offset(r, chunk & 7)) = v;
+      if (lane == 0) mbar_arrive(&bars[C_P_READY + w]);
+      // ---- dS^T = P^T o (dP^T - D)
+      if (!mbar_wait_warp(&bars[C_DP_FULL + w], k & 1, p.status, &abort_flag)) {
+        ok = false;
+        break;
       }
+      tc_fence_after_sync();
+      uint32_t ds_pack[kSub / 2];
+      {
+        float a[32], b[32];
+        tmem_ld32x2(tmem + lane_base + colDP, tmem + lane_base + colDP + 32, a, b);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          ds_pack[e / 2] = pack_bf16x2(pr[e] * (a[e] - Dq[e]), pr[e + 1] * (a[e + 1] - Dq[e + 1]));
+          ds_pack[16 + e / 2] = pack_bf16x2(pr[32 + e] * (b[e] - Dq[32 + e]),
+                                            pr[33 + e] * (b[e + 1] - Dq[33 + e]));
+        }
+      }
+      if (!mbar_wait_warp(&bars[C_X_FREE + w], k & 1, p.status, &abort_flag)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int chunk = 0; chunk < kSub / 8; ++chunk)
+        *reinterpret_cast<uint4*>(xbase + sw128_offset(r, chunk)) =
+            make_uint4(ds_pack[chunk * 4 + 0], ds_pack[chunk * 4 + 1], ds_pack[chunk * 4 + 2],
+                       ds_pack[chunk * 4 + 3]);
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[C_DS_READY]);
-      // ---- drain the dQ tile: this thread owns query row q0 + r
-      if (!mbar_wait_warp(&bars[C_DQ_FULL], i & 1, p.status, &abort_flag)) { ok = false; break; }
+      if (lane == 0) mbar_arrive(&bars[C_DS_READY + w]);
+      // ---- dQ^T: thread r owns head-dim row r of the 64 query columns
+      if (!mbar_wait_warp(&bars[C_DQ_FULL + w], k & 1, p.status, &abort_flag)) {
+        ok = false;
+        break;
+      }
       tc_fence_after_sync();
-      {
-        const int qpos = q0 + r;
+      float dq[kSub];
+      tmem_ld32x2(tmem + lane_base + colDP, tmem + lane_base + colDP + 32, dq, dq + 32);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C_DQ_FREE + w]);
+      if (r < D) {
         float* dst = p.dq_acc +
-                     (((static_cast<int64_t>(qs) * p.batch + bz) * p.L + qpos) * p.Hq + h) * D;
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          float v[32];
-          tmem_ld32(tmem + lane_base + 0 + ch * 32, v);
-          if (qpos < p.L) {
+                     (((static_cast<int64_t>(qs) * p.batch + bz) * p.L + q0) * p.Hq + h) * D + r;
+        const int64_t row_stride = static_cast<int64_t>(p.Hq) * D;
+        const int nvalid = p.L - q0 < kSub ? p.L - q0 : kSub;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              atomicAdd(reinterpret_cast<float4*>(dst + ch * 32 + e),
-                        make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]));
+        for (int c = 0; c < kSub; ++c)
+          if (c < nvalid) atomicAdd(dst + c * row_stride, dq[c]);
+      }
+    }
+    // ---- epilogue (stream 0): dV, dK rows of this key tile
+    if (w == 0) {
+      __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(k_stream ? p.dv[1] : p.dv[0]) +
+                          ((static_cast<int64_t>(bz) * p.L + kpos) * p.Hkv + kvh) * D;
+      __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(k_stream ? p.dk[1] : p.dk[0]) +
+                          ((static_cast<int64_t>(bz) * p.L + kpos) * p.Hkv + kvh) * D;
+      if (n_sub == 0) {
+        if (k_valid) {
+          for (int c = 0; c < D; c += 8) {
+            *reinterpret_cast<uint4*>(dv + c) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(dk + c) = make_uint4(0, 0, 0, 0);
           }
         }
-      }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[C_DQ_FREE]);
-    }
-    // ---- epilogue: dV, dK rows of this key tile
-    __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(k_stream ? p.dv[1] : p.dv[0]) +
-                        ((static_cast<int64_t>(bz) * p.L + kpos) * p.Hkv + kvh) * D;
-    __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(k_stream ? p.dk[1] : p.dk[0]) +
-                        ((static_cast<int64_t>(bz) * p.L + kpos) * p.Hkv + kvh) * D;
-    if (n_iters == 0) {
-      if (k_valid) {
-        for (int c = 0; c < D; c += 8) {
-          *reinterpret_cast<uint4*>(dv + c) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(dk + c) = make_uint4(0, 0, 0, 0);
-        }
-      }
-    } else if (ok && mbar_wait_warp(&bars[C_ACC_DONE], 0, p.status, &abort_flag)) {
-      tc_fence_after_sync();
+      } else if (ok && mbar_wait_warp(&bars[C_ACC_DONE], 0, p.status, &abort_flag)) {
+        tc_fence_after_sync();
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        __nv_bfloat16* dst = half ? dk : dv;
-        const uint32_t col = half ? Lay::kColDK : Lay::kColDV;
-        const float mul = half ? p.scale : 1.f;
+        for (int half = 0; half < 2; ++half) {
+          __nv_bfloat16* dstp = half ? dk : dv;
+          const uint32_t col = half ? Lay::kColDK : Lay::kColDV;
+          const float mul = half ? p.scale : 1.f;
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          float v[32];
-          tmem_ld32(tmem + lane_base + col + ch * 32, v);
-          if (k_valid) {
+          for (int ch = 0; ch < D / 32; ++ch) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + col + ch * 32, v);
+            if (k_valid) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 u;
-              u.x = pack_bf16x2(v[e] * mul, v[e + 1] * mul);
-              u.y = pack_bf16x2(v[e + 2] * mul, v[e + 3] * mul);
-              u.z = pack_bf16x2(v[e + 4] * mul, v[e + 5] * mul);
-              u.w = pack_bf16x2(v[e + 6] * mul, v[e + 7] * mul);
-              *reinterpret_cast<uint4*>(dst + ch * 32 + e) = u;
+              for (int e = 0; e < 32; e += 8) {
+                uint4 u;
+                u.x = pack_bf16x2(v[e] * mul, v[e + 1] * mul);
+                u.y = pack_bf16x2(v[e + 2] * mul, v[e + 3] * mul);
+                u.z = pack_bf16x2(v[e + 4] * mul, v[e + 5] * mul);
+                u.w = pack_bf16x2(v[e + 6] * mul, v[e + 7] * mul);
+                *reinterpret_cast<uint4*>(dstp + ch * 32 + e) = u;
+              }
             }
           }
         }
@@ -433,11 +518,16 @@ static cudaError_t launch_bwd_d(const CUtensorMap* maps, const BwdParams& p, int
   const int64_t grid = static_cast<int64_t>(n_tasks) * p.Hkv * p.batch;
   if (grid <= 0) return cudaSuccess;
   bwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, Lay::kDynSmem, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], p);
+      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], p);
   return cudaGetLastError();
 }
 
+// Rows of one TMA box for the query-side maps (Q, dO) and the LSE/D maps.
+int bwd_query_box_rows() { return kSub; }
+
 // maps: q_clean, q_corr, k_clean, k_corr, v_clean, v_corr, do_clean, do_corr
+//       (query-side maps with 64-row boxes), lse ({L, batch*2*Hq} fp32) and
+//       dsum ({L, 2*batch*Hq} fp32) with 64-position boxes
 cudaError_t launch_bwd(int d, const CUtensorMap* maps, const BwdParams& p, int n_tasks,
                        cudaStream_t stream) {
   if (d == 128) return launch_bwd_d<128>(maps, p, n_tasks, stream);

@@ -87,9 +87,26 @@ struct TileWalk {
   }
 };
 
-__device__ __forceinline__ bool mask_allows(int q_stream, int k_stream, int qb, int kb) {
-  if (q_stream == 0) return k_stream == 0 && kb <= qb;
-  return k_stream == 0 ? (kb < qb) : (kb == qb);
+// Key positions [lo, hi) of copy k_stream that a query of block qb of copy
+// q_stream may read: clean queries read clean keys of blocks <= qb;
+// corrupted queries read clean keys of blocks < qb and the corrupted keys of
+// their own block.
+__device__ __forceinline__ void allowed_key_range(int q_stream, int k_stream, int qb, int M, int L,
+                                                  bool row_valid, int& lo, int& hi) {
+  lo = 0;
+  if (!row_valid || (q_stream == 0 && k_stream == 1)) {
+    hi = 0;
+    return;
+  }
+  if (q_stream == 0) {
+    hi = (qb + 1) * M;
+  } else if (k_stream == 0) {
+    hi = qb * M;
+  } else {
+    lo = qb * M;
+    hi = (qb + 1) * M;
+  }
+  hi = min(hi, L);
 }
 
 template <int D>
@@ -267,20 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ragged = (static_cast<int64_t>(w.t) + 1) * kTile > p.L;
       float mx = -INFINITY;
       if ((w.flags & 1) || ragged || !row_valid) {
-        // key block id walks up by one every M columns: no per-element division
-        const int k0 = w.t * kTile;
-        int kb = k0 / p.M;
-        int kr = k0 - kb * p.M;
-        const int kvalid = p.L - k0;
+        // the allowed keys of this query row form one range [lo, hi)
+        int lo, hi;
+        allowed_key_range(q_stream, w.stream, qb, p.M, p.L, row_valid, lo, hi);
+        lo -= w.t * kTile;
+        hi -= w.t * kTile;
 #pragma unroll
         for (int c = 0; c < kTile; ++c) {
-          const bool allow = row_valid && c < kvalid && mask_allows(q_stream, w.stream, qb, kb);
-          s[c] = allow ? s[c] * sl2 : -INFINITY;
+          s[c] = (c >= lo && c < hi) ? s[c] * sl2 : -INFINITY;
           mx = fmaxf(mx, s[c]);
-          if (++kr == p.M) {
-            kr = 0;
-            ++kb;
-          }
         }
       } else {
 #pragma unroll

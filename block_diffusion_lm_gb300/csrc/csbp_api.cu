@@ -17,6 +17,7 @@ cudaError_t launch_fwd(int d, const CUtensorMap* maps, const FwdParams& p, int n
                        cudaStream_t stream);
 cudaError_t launch_bwd(int d, const CUtensorMap* maps, const BwdParams& p, int n_tasks,
                        cudaStream_t stream);
+int bwd_query_box_rows();
 cudaError_t launch_lse_merge(const MergeArgs& a, int n_parts, int64_t rows, int Hq, int d,
                              void* o_out, float* z_out, cudaStream_t stream);
 cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, float* Dsum, float* dq_acc,
@@ -48,19 +49,35 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D map over a bf16 [batch][L][H][d] tensor viewed as {H*d, L, batch};
-// box = 64 elements (128 B, one swizzle row) x 128 rows x 1.
-bool make_map(CUtensorMap* m, const void* base, int64_t H, int d, int64_t L, int64_t batch) {
+// box = 64 elements (128 B, one swizzle row) x box_rows rows x 1.
+bool make_map(CUtensorMap* m, const void* base, int64_t H, int d, int64_t L, int64_t batch,
+              int box_rows = kTile) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(H * d), static_cast<cuuint64_t>(L),
                         static_cast<cuuint64_t>(batch)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(H * d * 2),
                            static_cast<cuuint64_t>(L * H * d * 2)};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2-D map over an fp32 [rows][L] array; box = box_len consecutive positions
+// of one row (positions >= L read as zero).  Needs L % 4 == 0 (16-byte rows).
+bool make_map_rows_f32(CUtensorMap* m, const void* base, int64_t L, int64_t rows, int box_len) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(L * 4)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_len), 1};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -226,6 +243,7 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
   csbp_status st = validate_problem(problem);
   if (st != CSBP_OK) return st;
   if (problem->tile_q != kTile) return CSBP_ERR_UNSUPPORTED;
+  if (problem->L % 4 != 0) return CSBP_ERR_UNSUPPORTED;  // LSE / D rows are TMA-loaded
   if ((st = check_inputs(problem, in)) != CSBP_OK) return st;
   const bool hc = problem->has_clean_queries != 0;
   if (!work_dev || !info || !o_corr || !lse || !do_corr || !dq_corr || !dk_clean || !dv_clean ||
@@ -241,22 +259,25 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   const csbp_problem& p = *problem;
 
-  CUtensorMap maps[8];
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* dsum = reinterpret_cast<float*>(ws + wl.dsum);
+  float* dq_acc = reinterpret_cast<float*>(ws + wl.dq_acc);
+
+  CUtensorMap maps[10];
   const void* qc = in->q_clean ? in->q_clean : in->q_corr;
   const void* dc = do_clean ? do_clean : do_corr;
-  if (!make_map(&maps[0], qc, p.Hq, p.d, p.L, p.batch) ||
-      !make_map(&maps[1], in->q_corr, p.Hq, p.d, p.L, p.batch) ||
+  const int qbox = bwd_query_box_rows();
+  if (!make_map(&maps[0], qc, p.Hq, p.d, p.L, p.batch, qbox) ||
+      !make_map(&maps[1], in->q_corr, p.Hq, p.d, p.L, p.batch, qbox) ||
       !make_map(&maps[2], in->k_clean, p.Hkv, p.d, p.L, p.batch) ||
       !make_map(&maps[3], in->k_corr, p.Hkv, p.d, p.L, p.batch) ||
       !make_map(&maps[4], in->v_clean, p.Hkv, p.d, p.L, p.batch) ||
       !make_map(&maps[5], in->v_corr, p.Hkv, p.d, p.L, p.batch) ||
-      !make_map(&maps[6], dc, p.Hq, p.d, p.L, p.batch) ||
-      !make_map(&maps[7], do_corr, p.Hq, p.d, p.L, p.batch))
+      !make_map(&maps[6], dc, p.Hq, p.d, p.L, p.batch, qbox) ||
+      !make_map(&maps[7], do_corr, p.Hq, p.d, p.L, p.batch, qbox) ||
+      !make_map_rows_f32(&maps[8], lse, p.L, static_cast<int64_t>(p.batch) * 2 * p.Hq, qbox) ||
+      !make_map_rows_f32(&maps[9], dsum, p.L, static_cast<int64_t>(p.batch) * 2 * p.Hq, qbox))
     return CSBP_ERR_CUDA;
-
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* dsum = reinterpret_cast<float*>(ws + wl.dsum);
-  float* dq_acc = reinterpret_cast<float*>(ws + wl.dq_acc);
   const int64_t rows = static_cast<int64_t>(p.batch) * p.L;
   const int64_t stream_elems = rows * p.Hq * p.d;
   const void* o_s[2] = {o_clean, o_corr};

@@ -157,6 +157,8 @@ csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inputs* in,
  * contributions from clean queries of the same or later blocks and from
  * corrupted queries of later blocks; corrupted dK/dV only from queries of
  * their own block.  do_clean / dq_clean may be NULL without clean queries.
+ * Needs L % 4 == 0 (the LSE and D rows are TMA-loaded), else
+ * CSBP_ERR_UNSUPPORTED.
  * workspace: device, >= csbp_workspace_bytes(problem, 1).               */
 csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inputs* in,
                           const void* work_dev, const csbp_schedule_info* info,
