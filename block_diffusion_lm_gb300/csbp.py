@@ -66,6 +66,9 @@ def lib():
                                     sz, vp]
         L.csbp_attn_bwd.argtypes = [P(Problem), P(Inputs), vp, P(ScheduleInfo), vp, vp, vp, vp,
                                     vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.csbp_attn_bwd_noalloc.argtypes = [P(Problem), P(Inputs), vp, P(ScheduleInfo), vp, vp,
+                                            vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.csbp_attn_bwd_noalloc.restype = ctypes.c_int
         L.csbp_lse_merge.argtypes = [i32, P(vp), P(vp), i64, i32, i32, vp, vp, vp]
         L.csbp_check_status.argtypes = [vp, vp]
         L.csbp_status_string.argtypes = [ctypes.c_int]
@@ -154,6 +157,22 @@ def attn_bwd(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse, do_cle
                              _ptr(grads["dv_corr"]), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check("csbp_attn_bwd", st)
+
+
+def attn_bwd_noalloc(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse, do_clean,
+                     do_corr, grads: dict, stream=None):
+    """csbp_attn_bwd_noalloc: the backward with the library's own fixed
+    scratch instead of a caller workspace (for callers that cannot allocate
+    device memory; calls on one device must not overlap)."""
+    inp = Inputs(*(_ptr(inputs.get(n)) for n in
+                   ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")))
+    st = lib().csbp_attn_bwd_noalloc(ctypes.byref(problem), ctypes.byref(inp), _ptr(work_dev),
+                                     ctypes.byref(info), _ptr(o_clean), _ptr(o_corr), _ptr(lse),
+                                     _ptr(do_clean), _ptr(do_corr), _ptr(grads.get("dq_clean")),
+                                     _ptr(grads["dq_corr"]), _ptr(grads["dk_clean"]),
+                                     _ptr(grads["dv_clean"]), _ptr(grads["dk_corr"]),
+                                     _ptr(grads["dv_corr"]), _stream_ptr(stream))
+    _check("csbp_attn_bwd_noalloc", st)
 
 
 def lse_merge(o_parts, lse_parts, o_out, lse_out, stream=None):

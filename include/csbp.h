@@ -167,6 +167,31 @@ csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inputs* in,
                           void* dq_corr, void* dk_clean, void* dv_clean, void* dk_corr,
                           void* dv_corr, void* workspace, size_t ws_bytes, void* stream);
 
+/* Backward without any workspace argument, for callers that cannot allocate
+ * device memory (plugin or custom-op interfaces that receive only their
+ * input and output buffers, runtimes whose memory pool forbids outside
+ * allocations, paths that cannot afford cudaMalloc's implicit device
+ * synchronisation).  This entry point has no counterpart on the method's
+ * pages; it is a deployment convenience of this library.
+ * Same arguments, layouts and results as csbp_attn_bwd, minus the
+ * workspace.  Its scratch is one fixed 64 MiB array in device global memory
+ * that every GPU loading the library holds until the process exits; a
+ * problem whose csbp_workspace_bytes(problem, 1) exceeds 64 MiB is rejected
+ * with CSBP_ERR_WORKSPACE before anything is enqueued.  It allocates and
+ * frees nothing.  The first call on a device looks up the array's device
+ * address (make that first call before any stream capture).  All calls on a
+ * device share the array and it keeps the last call's contents: each call
+ * clears the part that must start at zero, and calls that can overlap on the
+ * GPU (for example on two streams without ordering) race and corrupt each
+ * other's results.  A device wait that timed out is not reported for this
+ * variant (csbp_check_status needs the workspace).                       */
+csbp_status csbp_attn_bwd_noalloc(const csbp_problem* problem, const csbp_inputs* in,
+                                  const void* work_dev, const csbp_schedule_info* info,
+                                  const void* o_clean, const void* o_corr, const float* lse,
+                                  const void* do_clean, const void* do_corr, void* dq_clean,
+                                  void* dq_corr, void* dk_clean, void* dv_clean, void* dk_corr,
+                                  void* dv_corr, void* stream);
+
 /* Exact log-sum-exp merge of n_parts partial attentions over disjoint key
  * sets (blog section "在线 softmax 合并"): m = max_s z_s, w_s = exp(z_s - m),
  * O = sum_s w_s O_s / sum_s w_s, z = m + log(sum_s w_s), all in fp32; a part
