@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--impl", default="csbp", choices=["csbp", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer end-to-end leg (auxiliary measurements)")
     ap.add_argument("--L", type=int, default=None,
                     help="override the sequence length (profiling captures of a smaller case)")
     return ap.parse_args()
@@ -275,6 +277,49 @@ def main():
     value = world * flops / (ms_per_step * 1e-3) / 1e12
 
     # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, t, attn, out, grads, stream, dev, world, flops, in_bytes)
+
+    pk = peaks()
+    bwd_avg = statistics.mean(bwd_ms)
+    fwd_avg = statistics.mean(fwd_ms)
+    achieved = w.useful_bwd_flops() / (bwd_avg * 1e-3) / 1e12
+    peak = pk["bf16_sustained"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(config, l2=f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB resident "
+                                  f"vs {L2_BYTES / 2**20:.0f} MiB L2); no flush"),
+        "pct_of_bf16_peak": value / world / pk["bf16_sustained"],
+        "fwd_ms": fwd_avg, "bwd_ms": bwd_avg,
+        "fwd_tflops": w.useful_fwd_flops() / (fwd_avg * 1e-3) / 1e12,
+        "bwd_tflops": achieved,
+        "roofline": {"bound": "tensor", "kernel": f"bwd_kernel<{w.d}> (csbp_attn_bwd call)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "peak_source": f"bf16_tflops_sustained of {pk['source']}",
+                     "traffic": None},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step(w) * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, t, attn, out, grads, stream, dev, world, flops, in_bytes):
+    """Same step through the public API from pinned host inputs, with the
+    outputs and gradients copied back, all inside the timed region."""
+    import torch
+    import torch.distributed as dist
+
     host_in = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in t.items()}
     dev_in = {k: (torch.empty_like(v) if v is not None else None) for k, v in t.items()}
     res = [x for x in (*out, *grads.values()) if x is not None]
@@ -307,39 +352,8 @@ def main():
         dist.all_reduce(x, op=dist.ReduceOp.MAX)
         e2e_ms = x.item()
     e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
-
-    pk = peaks()
-    bwd_avg = statistics.mean(bwd_ms)
-    fwd_avg = statistics.mean(fwd_ms)
-    achieved = w.useful_bwd_flops() / (bwd_avg * 1e-3) / 1e12
-    peak = pk["bf16_sustained"]
-    line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": dict(config, l2=f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB resident "
-                                  f"vs {L2_BYTES / 2**20:.0f} MiB L2); no flush"),
-        "pct_of_bf16_peak": value / world / pk["bf16_sustained"],
-        "fwd_ms": fwd_avg, "bwd_ms": bwd_avg,
-        "fwd_tflops": w.useful_fwd_flops() / (fwd_avg * 1e-3) / 1e12,
-        "bwd_tflops": achieved,
-        "roofline": {"bound": "tensor", "kernel": f"bwd_kernel<{w.d}> (csbp_attn_bwd call)",
-                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak,
-                     "peak_source": f"bf16_tflops_sustained of {pk['source']}",
-                     "traffic": None},
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": in_bytes,
-                "d2h_bytes_per_step": out_bytes},
-        "gpu_launches": launches_per_step(w) * args.steps,
-        "clocks": clocks,
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(w, args.cpu_seconds)
-    if rank == 0:
-        print(json.dumps(line))
-    if world > 1:
-        dist.destroy_process_group()
+    return {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": in_bytes,
+            "d2h_bytes_per_step": out_bytes}
 
 
 if __name__ == "__main__":
