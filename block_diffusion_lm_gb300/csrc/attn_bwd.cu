@@ -14,20 +14,23 @@
 // query tile is processed as two 64-row sub-tiles by two compute warpgroups
 // that alternate, so the tensor core works on one sub-tile while the other
 // warpgroup computes exponentials.  Roles (384 threads):
-//   warp 0 lane 0  TMA producer: K, V once; per sub-tile Q (4 stages) with its
-//                  LSE and D slices, and dO (3 stages)
+//   warp 0 lane 0  TMA producer: K, V once; per sub-tile Q (3 stages) with its
+//                  LSE and D slices, and dO (2 stages)
 //   warp 1 lane 0  MMA issuer, per sub-tile s (stream w = s & 1):
-//                    dV += P_s^T dO_s;  dK += dS_s^T Q_s;  dQ_s^T = K^T dS_s^T
+//                    dV += P_s^T dO_s   (P^T read from TMEM)
+//                    dK += dS_s^T Q_s;  dQ_s^T = K^T dS_s^T  (dS^T from smem)
 //                    then dP^T_{s+1} = V dO_{s+1}^T and S^T_{s+2} = K Q_{s+2}^T
 //   warps 4..7 / 8..11  compute streams 0 / 1: thread t owns key row t (TMEM
-//                  lane t); builds P^T and dS^T (fp32 math, bf16 operands)
-//                  through the stream's 128B-swizzled shared tile, then copies
-//                  dQ^T (thread t = head-dim row t) out of TMEM and adds it to
-//                  the fp32 dQ accumulator: one warp-wide atomic add covers 32
-//                  consecutive head-dim elements (128 contiguous bytes).
-// TMEM columns: stream w has S^T at 128w and dP^T (then dQ^T) at 128w + 64;
-// dV at 256, dK at 256 + d.  For d = 64 the dQ^T MMA runs with M = 128 and
-// the upper 64 rows of K^T read a zero tile.
+//                  lane t).  It turns S^T into P^T (bf16, written back over
+//                  its own S^T columns of TMEM) and dP^T into dS^T (bf16,
+//                  into the stream's 128B-swizzled shared tile: the K-major A
+//                  operand of dK and the MN-major B operand of dQ^T).  Then it
+//                  copies dQ^T (thread t = head-dim row t) out of TMEM into a
+//                  shared staging tile, from which one TMA bulk reduce-add per
+//                  32 query rows adds it into the fp32 dQ accumulator.
+// TMEM columns: stream w has S^T (then P^T) at 128w and dP^T (then dQ^T) at
+// 128w + 64; dV at 256, dK at 256 + d.  For d = 64 the dQ^T MMA runs with
+// M = 128 and the upper 64 rows of K^T read a zero tile.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -40,8 +43,9 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kSub = 64;          // query rows per sub-tile
-constexpr int kQStages = 4;
-constexpr int kDOStages = 3;
+constexpr int kQStages = 3;
+constexpr int kDOStages = 2;
+constexpr int kStageRows = 32;    // query rows per dQ reduce-add
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -50,7 +54,8 @@ struct BwdLayout {
   static constexpr int kKVBox = kTile * 128;         // one 64-column box of K/V
   static constexpr int kSubBytes = kSub * D * 2;     // Q or dO sub-tile
   static constexpr int kSubBox = kSub * 128;         // one 64-column box of a sub-tile
-  static constexpr int kXBytes = kTile * kSub * 2;   // P^T / dS^T of one stream
+  static constexpr int kXBytes = kTile * kSub * 2;   // dS^T of one stream
+  static constexpr int kStageBytes = kStageRows * D * 4;  // fp32 dQ rows of one stream
   static constexpr int kStatBytes = 2 * kSub * 4;    // LSE and D of one sub-tile
   static constexpr int kK = 0;
   static constexpr int kV = kK + kKVBytes;
@@ -58,7 +63,8 @@ struct BwdLayout {
   static constexpr int kQ = kZero + (D == 64 ? kKVBox : 0);
   static constexpr int kDO = kQ + kQStages * kSubBytes;
   static constexpr int kX = kDO + kDOStages * kSubBytes;
-  static constexpr int kStat = kX + 2 * kXBytes;
+  static constexpr int kStage = kX + 2 * kXBytes;
+  static constexpr int kStat = kStage + 2 * kStageBytes;
   static constexpr int kBytes = kStat + kQStages * kStatBytes;
   static constexpr int kDynSmem = kBytes + 1024;
   static constexpr uint32_t kColDV = 256;
@@ -71,15 +77,17 @@ enum BwdBar {
   C_Q_EMPTY = C_Q_FULL + kQStages,   // [kQStages]
   C_DO_FULL = C_Q_EMPTY + kQStages,  // [kDOStages]
   C_DO_EMPTY = C_DO_FULL + kDOStages,
-  C_S_FULL = C_DO_EMPTY + kDOStages,  // per stream [2]
+  C_S_FULL = C_DO_EMPTY + kDOStages,  // per stream [2] from here on
   C_DP_FULL = C_S_FULL + 2,
   C_P_READY = C_DP_FULL + 2,
-  C_X_FREE = C_P_READY + 2,
-  C_DS_READY = C_X_FREE + 2,
-  C_X_FREE2 = C_DS_READY + 2,
-  C_DQ_FULL = C_X_FREE2 + 2,
+  C_PV_DONE = C_P_READY + 2,
+  C_DS_READY = C_PV_DONE + 2,
+  C_X_FREE = C_DS_READY + 2,
+  C_DQ_FULL = C_X_FREE + 2,
   C_DQ_FREE = C_DQ_FULL + 2,
-  C_ACC_DONE = C_DQ_FREE + 2,
+  C_STAGE_FULL = C_DQ_FREE + 2,
+  C_STAGE_FREE = C_STAGE_FULL + 2,
+  C_ACC_DONE = C_STAGE_FREE + 2,
   C_DRAIN,
   C_COUNT
 };
@@ -152,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap tm_do0,
                const __grid_constant__ CUtensorMap tm_do1,
                const __grid_constant__ CUtensorMap tm_lse,
-               const __grid_constant__ CUtensorMap tm_dsum, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_dsum,
+               const __grid_constant__ CUtensorMap tm_dqacc, const BwdParams p) {
   using Lay = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -180,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C_COUNT; ++i) {
       const bool per_warp = (i >= C_P_READY && i < C_P_READY + 2) ||
                             (i >= C_DS_READY && i < C_DS_READY + 2) ||
-                            (i >= C_DQ_FREE && i < C_DQ_FREE + 2);
+                            (i >= C_DQ_FREE && i < C_DQ_FREE + 2) ||
+                            (i >= C_STAGE_FULL && i < C_STAGE_FULL + 2);
       mbar_init(&bars[i], per_warp ? 4 : 1);
     }
     abort_flag = 0;
@@ -295,16 +305,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w = s & 1;
       const int k = s >> 1;
       const uint32_t xw = sX + w * Lay::kXBytes;
-      // ---- finish sub-tile s
+      // ---- dV += P^T dO (P^T in TMEM over the stream's S^T columns)
       if (!mbar_wait(&bars[C_P_READY + w], k & 1, p.status, &abort_flag)) break;
       tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < kSub / 16; ++kk)
-        umma_bf16_ss(tmem + Lay::kColDV, sdesc_sw128(xw + kk * 32, 16, 1024),
+        umma_bf16_ts(tmem + Lay::kColDV, tmem + w * 128 + kk * 8,
                      sdesc_sw128(dobuf(s) + kk * 2048, Lay::kSubBox, 1024), idesc_kd,
                      (s > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(&bars[C_X_FREE + w]);
+      umma_commit(&bars[C_PV_DONE + w]);
       umma_commit(&bars[C_DO_EMPTY + s % kDOStages]);
+      // ---- dK += dS^T Q; dQ^T = K^T dS^T
       if (!mbar_wait(&bars[C_DS_READY + w], k & 1, p.status, &abort_flag)) break;
       tc_fence_after_sync();
 #pragma unroll
@@ -312,7 +323,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_bf16_ss(tmem + Lay::kColDK, sdesc_sw128(xw + kk * 32, 16, 1024),
                      sdesc_sw128(qbuf(s) + kk * 2048, Lay::kSubBox, 1024), idesc_kd,
                      (s > 0 || kk > 0) ? 1u : 0u);
-      // dQ^T = K^T dS^T: A = K tile read MN-major (M = d), B = dS^T (N = 64 queries)
       const uint32_t a_lbo = (D == 64) ? static_cast<uint32_t>(Lay::kZero - Lay::kK) : Lay::kKVBox;
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk)
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      sdesc_sw128(xw + kk * 2048, Lay::kXBytes, 1024), idesc_q, kk > 0 ? 1u : 0u);
       umma_commit(&bars[C_DQ_FULL + w]);
       umma_commit(&bars[C_Q_EMPTY + s % kQStages]);
-      umma_commit(&bars[C_X_FREE2 + w]);
+      umma_commit(&bars[C_X_FREE + w]);
       // ---- dP^T of sub-tile s+1 (other stream; its columns held dQ^T_{s-1})
       if (s + 1 < n_sub) {
         const int w1 = w ^ 1;
@@ -331,9 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_kq<D>(tmem + w1 * 128 + 64, sV, dobuf(s + 1));
         umma_commit(&bars[C_DP_FULL + w1]);
       }
-      // ---- S^T of sub-tile s+2 (this stream; read before P_READY_s)
+      // ---- S^T of sub-tile s+2 (this stream): its columns held P^T_s, which
+      //      dV_s has finished reading once PV_DONE completes
       if (s + 2 < n_sub) {
-        if (!wait_q(s + 2)) break;
+        if (!wait_q(s + 2) || !mbar_wait(&bars[C_PV_DONE + w], k & 1, p.status, &abort_flag)) break;
         tc_fence_after_sync();
         issue_kq<D>(tmem + w * 128, sK, qbuf(s + 2));
         umma_commit(&bars[C_S_FULL + w]);
@@ -346,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ===================== compute streams
     const int w = (warp >= 8) ? 1 : 0;
     const int r = threadIdx.x - 128 * (w + 1);  // key row (TMEM lane)
+    const bool leader = (warp & 3) == 0;        // this warp issues the dQ reduce-adds
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t colS = w * 128, colDP = w * 128 + 64;
     const int kpos = k_tile * kTile + r;
@@ -353,10 +365,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kb = k_valid ? kpos / p.M : -1;
     const float sl2 = p.scale_log2;
     uint8_t* xbase = smem + Lay::kX + w * Lay::kXBytes;
+    float* stage = reinterpret_cast<float*>(smem + Lay::kStage + w * Lay::kStageBytes);
     const bool k_ragged = (k_tile + 1) * kTile > p.L;
     QWalk wk;
     wk.start(segs, n_segs);
     bool ok = true;
+    int uses = 0;  // dQ staging uses of this stream
     for (int s = w; s < n_sub; s += 2, wk.next()) {
       const int k = s >> 1;
       const int qs = wk.stream;
@@ -365,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qst = s % kQStages;
       if (!mbar_wait_warp(&bars[C_S_FULL + w], k & 1, p.status, &abort_flag) ||
           !mbar_wait_warp(&bars[C_Q_FULL + qst], (s / kQStages) & 1, p.status, &abort_flag) ||
-          (k > 0 && !mbar_wait_warp(&bars[C_X_FREE2 + w], (k - 1) & 1, p.status, &abort_flag))) {
+          (k > 0 && !mbar_wait_warp(&bars[C_X_FREE + w], (k - 1) & 1, p.status, &abort_flag))) {
         ok = false;
         break;
       }
@@ -373,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* lse = reinterpret_cast<const float*>(smem + Lay::kStat + qst * Lay::kStatBytes);
       const float* Dq = lse + kSub;
       const bool masked = (wk.flags & 1) || k_ragged || (q0 + kSub > p.L);
-      // ---- P^T = exp(S^T scale - LSE)
+      // ---- P^T = exp(S^T scale - LSE), written back to TMEM as bf16 pairs
       float pr[kSub];
       tmem_ld32x2(tmem + lane_base + colS, tmem + lane_base + colS + 32, pr, pr + 32);
       if (masked) {
@@ -391,45 +405,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kSub; ++c) pr[c] = ex2_approx(fmaf(pr[c], sl2, -lse[c] * kLog2e));
       }
+      {
+        float packed[32];
 #pragma unroll
-      for (int chunk = 0; chunk < kSub / 8; ++chunk) {
-        uint4 v;
-        v.x = pack_bf16x2(pr[chunk * 8 + 0], pr[chunk * 8 + 1]);
-        v.y = pack_bf16x2(pr[chunk * 8 + 2], pr[chunk * 8 + 3]);
-        v.z = pack_bf16x2(pr[chunk * 8 + 4], pr[chunk * 8 + 5]);
-        v.w = pack_bf16x2(pr[chunk * 8 + 6], pr[chunk * 8 + 7]);
-        *reinterpret_cast<uint4*>(xbase + sw128_offset(r, chunk)) = v;
+        for (int c = 0; c < 32; ++c) packed[c] = __uint_as_float(pack_bf16x2(pr[2 * c], pr[2 * c + 1]));
+        tmem_st32(tmem + lane_base + colS, packed);
       }
-      fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C_P_READY + w]);
-      // ---- dS^T = P^T o (dP^T - D)
+      // ---- dS^T = P^T o (dP^T - D) into the shared tile
       if (!mbar_wait_warp(&bars[C_DP_FULL + w], k & 1, p.status, &abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      uint32_t ds_pack[kSub / 2];
       {
         float a[32], b[32];
         tmem_ld32x2(tmem + lane_base + colDP, tmem + lane_base + colDP + 32, a, b);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          ds_pack[e / 2] = pack_bf16x2(pr[e] * (a[e] - Dq[e]), pr[e + 1] * (a[e + 1] - Dq[e + 1]));
-          ds_pack[16 + e / 2] = pack_bf16x2(pr[32 + e] * (b[e] - Dq[32 + e]),
-                                            pr[33 + e] * (b[e + 1] - Dq[33 + e]));
+        for (int chunk = 0; chunk < kSub / 8; ++chunk) {
+          const float* dp = (chunk < 4) ? a + chunk * 8 : b + (chunk - 4) * 8;
+          const int c0 = chunk * 8;
+          uint4 v;
+          v.x = pack_bf16x2(pr[c0 + 0] * (dp[0] - Dq[c0 + 0]), pr[c0 + 1] * (dp[1] - Dq[c0 + 1]));
+          v.y = pack_bf16x2(pr[c0 + 2] * (dp[2] - Dq[c0 + 2]), pr[c0 + 3] * (dp[3] - Dq[c0 + 3]));
+          v.z = pack_bf16x2(pr[c0 + 4] * (dp[4] - Dq[c0 + 4]), pr[c0 + 5] * (dp[5] - Dq[c0 + 5]));
+          v.w = pack_bf16x2(pr[c0 + 6] * (dp[6] - Dq[c0 + 6]), pr[c0 + 7] * (dp[7] - Dq[c0 + 7]));
+          *reinterpret_cast<uint4*>(xbase + sw128_offset(r, chunk)) = v;
         }
       }
-      if (!mbar_wait_warp(&bars[C_X_FREE + w], k & 1, p.status, &abort_flag)) {
-        ok = false;
-        break;
-      }
-#pragma unroll
-      for (int chunk = 0; chunk < kSub / 8; ++chunk)
-        *reinterpret_cast<uint4*>(xbase + sw128_offset(r, chunk)) =
-            make_uint4(ds_pack[chunk * 4 + 0], ds_pack[chunk * 4 + 1], ds_pack[chunk * 4 + 2],
-                       ds_pack[chunk * 4 + 3]);
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
@@ -445,16 +450,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C_DQ_FREE + w]);
-      if (r < D) {
-        float* dst = p.dq_acc +
-                     (((static_cast<int64_t>(qs) * p.batch + bz) * p.L + q0) * p.Hq + h) * D + r;
-        const int64_t row_stride = static_cast<int64_t>(p.Hq) * D;
-        const int nvalid = p.L - q0 < kSub ? p.L - q0 : kSub;
+      // stage 32 query rows at a time ([row][d] fp32) and reduce-add them
 #pragma unroll
-        for (int c = 0; c < kSub; ++c)
-          if (c < nvalid) atomicAdd(dst + c * row_stride, dq[c]);
+      for (int half = 0; half < kSub / kStageRows; ++half, ++uses) {
+        if (uses > 0 &&
+            !mbar_wait_warp(&bars[C_STAGE_FREE + w], (uses - 1) & 1, p.status, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (r < D) {
+#pragma unroll
+          for (int c = 0; c < kStageRows; ++c) stage[c * D + r] = dq[half * kStageRows + c];
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C_STAGE_FULL + w]);
+        if (leader) {
+          if (!mbar_wait_warp(&bars[C_STAGE_FULL + w], uses & 1, p.status, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            tma_reduce_add_3d(&tm_dqacc, stage, h * D, q0 + half * kStageRows, qs * p.batch + bz);
+            bulk_commit_group();
+            bulk_wait_group_read<0>();
+            mbar_arrive(&bars[C_STAGE_FREE + w]);
+          }
+          __syncwarp();
+        }
       }
+      if (!ok) break;
     }
+    if (leader && lane == 0) bulk_wait_group<0>();  // reduce-adds complete before exit
     // ---- epilogue (stream 0): dV, dK rows of this key tile
     if (w == 0) {
       __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(k_stream ? p.dv[1] : p.dv[0]) +
@@ -518,16 +545,20 @@ static cudaError_t launch_bwd_d(const CUtensorMap* maps, const BwdParams& p, int
   const int64_t grid = static_cast<int64_t>(n_tasks) * p.Hkv * p.batch;
   if (grid <= 0) return cudaSuccess;
   bwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, Lay::kDynSmem, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], p);
+      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9],
+      maps[10], p);
   return cudaGetLastError();
 }
 
 // Rows of one TMA box for the query-side maps (Q, dO) and the LSE/D maps.
 int bwd_query_box_rows() { return kSub; }
+// Query rows of one dQ reduce-add box.
+int bwd_dq_box_rows() { return kStageRows; }
 
 // maps: q_clean, q_corr, k_clean, k_corr, v_clean, v_corr, do_clean, do_corr
 //       (query-side maps with 64-row boxes), lse ({L, batch*2*Hq} fp32) and
-//       dsum ({L, 2*batch*Hq} fp32) with 64-position boxes
+//       dsum ({L, 2*batch*Hq} fp32) with 64-position boxes, dq_acc
+//       ({Hq*d, L, 2*batch} fp32, box {d, 32, 1}, no swizzle)
 cudaError_t launch_bwd(int d, const CUtensorMap* maps, const BwdParams& p, int n_tasks,
                        cudaStream_t stream) {
   if (d == 128) return launch_bwd_d<128>(maps, p, n_tasks, stream);

@@ -18,6 +18,7 @@ cudaError_t launch_fwd(int d, const CUtensorMap* maps, const FwdParams& p, int n
 cudaError_t launch_bwd(int d, const CUtensorMap* maps, const BwdParams& p, int n_tasks,
                        cudaStream_t stream);
 int bwd_query_box_rows();
+int bwd_dq_box_rows();
 cudaError_t launch_lse_merge(const MergeArgs& a, int n_parts, int64_t rows, int Hq, int d,
                              void* o_out, float* z_out, cudaStream_t stream);
 cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, float* Dsum, float* dq_acc,
@@ -77,6 +78,25 @@ bool make_map_rows_f32(CUtensorMap* m, const void* base, int64_t L, int64_t rows
   cuuint32_t es[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D map over the fp32 dQ accumulator [2*batch][L][Hq][d] viewed as
+// {Hq*d, L, 2*batch}; box = d elements x box_rows rows x 1, no swizzle (the
+// target of the backward's TMA reduce-adds; rows >= L are clipped).
+bool make_map_dqacc(CUtensorMap* m, void* base, int64_t Hq, int d, int64_t L, int64_t planes,
+                    int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(Hq * d), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(Hq * d * 4),
+                           static_cast<cuuint64_t>(L * Hq * d * 4)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -263,10 +283,13 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
   float* dsum = reinterpret_cast<float*>(ws + wl.dsum);
   float* dq_acc = reinterpret_cast<float*>(ws + wl.dq_acc);
 
-  CUtensorMap maps[10];
+  CUtensorMap maps[11];
   const void* qc = in->q_clean ? in->q_clean : in->q_corr;
   const void* dc = do_clean ? do_clean : do_corr;
   const int qbox = bwd_query_box_rows();
+  if (!make_map_dqacc(&maps[10], dq_acc, p.Hq, p.d, p.L, 2 * static_cast<int64_t>(p.batch),
+                      bwd_dq_box_rows()))
+    return CSBP_ERR_CUDA;
   if (!make_map(&maps[0], qc, p.Hq, p.d, p.L, p.batch, qbox) ||
       !make_map(&maps[1], in->q_corr, p.Hq, p.d, p.L, p.batch, qbox) ||
       !make_map(&maps[2], in->k_clean, p.Hkv, p.d, p.L, p.batch) ||
