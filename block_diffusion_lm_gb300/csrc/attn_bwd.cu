@@ -140,15 +140,16 @@ __device__ __forceinline__ void allowed_query_range(int q_stream, int k_stream, 
 }
 
 // S^T (or dP^T) of one sub-tile: M = 128 key rows, N = 64 query rows, K = d.
+// a_kv / b_sub: K-major base descriptors of the key-side tile and the
+// query-side sub-tile.
 template <int D>
-__device__ __forceinline__ void issue_kq(uint32_t d_tmem, uint32_t a_kv, uint32_t b_sub) {
+__device__ __forceinline__ void issue_kq(uint32_t d_tmem, uint64_t a_kv, uint64_t b_sub) {
   using Lay = BwdLayout<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(128, kSub, false, false);
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
-    umma_bf16_ss(d_tmem, sdesc_sw128(a_kv + (k >> 2) * Lay::kKVBox + (k & 3) * 32, 16, 1024),
-                 sdesc_sw128(b_sub + (k >> 2) * Lay::kSubBox + (k & 3) * 32, 16, 1024), idesc,
-                 k > 0 ? 1u : 0u);
+    umma_bf16_ss(d_tmem, sdesc_step(a_kv, (k >> 2) * Lay::kKVBox + (k & 3) * 32),
+                 sdesc_step(b_sub, (k >> 2) * Lay::kSubBox + (k & 3) * 32), idesc, k > 0 ? 1u : 0u);
   }
 }
 
@@ -285,18 +286,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_do = [&](int s) {
       return mbar_wait(&bars[C_DO_FULL + s % kDOStages], (s / kDOStages) & 1, p.status, &abort_flag);
     };
+    // base descriptors of the CTA-resident key-side tiles
+    const uint64_t k_kmaj = sdesc_sw128(sK, 16, 1024);   // K as K-major A (S^T)
+    const uint64_t v_kmaj = sdesc_sw128(sV, 16, 1024);   // V as K-major A (dP^T)
+    const uint64_t k_mn = sdesc_sw128(                   // K^T as MN-major A (dQ^T)
+        sK, (D == 64) ? static_cast<uint32_t>(Lay::kZero - Lay::kK) : Lay::kKVBox, 1024);
     bool ok = mbar_wait(&bars[C_KV_FULL], 0, p.status, &abort_flag) && wait_q(0) && wait_do(0);
     if (ok) {
       tc_fence_after_sync();
-      issue_kq<D>(tmem + 0, sK, qbuf(0));
+      issue_kq<D>(tmem + 0, k_kmaj, sdesc_sw128(qbuf(0), 16, 1024));
       umma_commit(&bars[C_S_FULL + 0]);
-      issue_kq<D>(tmem + 64, sV, dobuf(0));
+      issue_kq<D>(tmem + 64, v_kmaj, sdesc_sw128(dobuf(0), 16, 1024));
       umma_commit(&bars[C_DP_FULL + 0]);
       if (n_sub > 1) {
         ok = wait_q(1);
         if (ok) {
           tc_fence_after_sync();
-          issue_kq<D>(tmem + 128, sK, qbuf(1));
+          issue_kq<D>(tmem + 128, k_kmaj, sdesc_sw128(qbuf(1), 16, 1024));
           umma_commit(&bars[C_S_FULL + 1]);
         }
       }
@@ -305,29 +311,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w = s & 1;
       const int k = s >> 1;
       const uint32_t xw = sX + w * Lay::kXBytes;
+      const uint32_t acc0 = s > 0 ? 1u : 0u;  // dV / dK accumulate after the first sub-tile
       // ---- dV += P^T dO (P^T in TMEM over the stream's S^T columns)
       if (!mbar_wait(&bars[C_P_READY + w], k & 1, p.status, &abort_flag)) break;
       tc_fence_after_sync();
+      {
+        const uint64_t b = sdesc_sw128(dobuf(s), Lay::kSubBox, 1024);  // dO as MN-major B
 #pragma unroll
-      for (int kk = 0; kk < kSub / 16; ++kk)
-        umma_bf16_ts(tmem + Lay::kColDV, tmem + w * 128 + kk * 8,
-                     sdesc_sw128(dobuf(s) + kk * 2048, Lay::kSubBox, 1024), idesc_kd,
-                     (s > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kSub / 16; ++kk)
+          umma_bf16_ts(tmem + Lay::kColDV, tmem + w * 128 + kk * 8, sdesc_step(b, kk * 2048),
+                       idesc_kd, kk > 0 ? 1u : acc0);
+      }
       umma_commit(&bars[C_PV_DONE + w]);
       umma_commit(&bars[C_DO_EMPTY + s % kDOStages]);
       // ---- dK += dS^T Q; dQ^T = K^T dS^T
       if (!mbar_wait(&bars[C_DS_READY + w], k & 1, p.status, &abort_flag)) break;
       tc_fence_after_sync();
+      {
+        const uint64_t a = sdesc_sw128(xw, 16, 1024);                  // dS^T as K-major A
+        const uint64_t b = sdesc_sw128(qbuf(s), Lay::kSubBox, 1024);   // Q as MN-major B
 #pragma unroll
-      for (int kk = 0; kk < kSub / 16; ++kk)
-        umma_bf16_ss(tmem + Lay::kColDK, sdesc_sw128(xw + kk * 32, 16, 1024),
-                     sdesc_sw128(qbuf(s) + kk * 2048, Lay::kSubBox, 1024), idesc_kd,
-                     (s > 0 || kk > 0) ? 1u : 0u);
-      const uint32_t a_lbo = (D == 64) ? static_cast<uint32_t>(Lay::kZero - Lay::kK) : Lay::kKVBox;
+        for (int kk = 0; kk < kSub / 16; ++kk)
+          umma_bf16_ss(tmem + Lay::kColDK, sdesc_step(a, kk * 32), sdesc_step(b, kk * 2048), idesc_kd,
+                       kk > 0 ? 1u : acc0);
+        const uint64_t bx = sdesc_sw128(xw, Lay::kXBytes, 1024);        // dS^T as MN-major B
 #pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk)
-        umma_bf16_ss(tmem + w * 128 + 64, sdesc_sw128(sK + kk * 2048, a_lbo, 1024),
-                     sdesc_sw128(xw + kk * 2048, Lay::kXBytes, 1024), idesc_q, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_bf16_ss(tmem + w * 128 + 64, sdesc_step(k_mn, kk * 2048), sdesc_step(bx, kk * 2048),
+                       idesc_q, kk > 0 ? 1u : 0u);
+      }
       umma_commit(&bars[C_DQ_FULL + w]);
       umma_commit(&bars[C_Q_EMPTY + s % kQStages]);
       umma_commit(&bars[C_X_FREE + w]);
@@ -338,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             !wait_do(s + 1))
           break;
         tc_fence_after_sync();
-        issue_kq<D>(tmem + w1 * 128 + 64, sV, dobuf(s + 1));
+        issue_kq<D>(tmem + w1 * 128 + 64, v_kmaj, sdesc_sw128(dobuf(s + 1), 16, 1024));
         umma_commit(&bars[C_DP_FULL + w1]);
       }
       // ---- S^T of sub-tile s+2 (this stream): its columns held P^T_s, which
@@ -346,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (s + 2 < n_sub) {
         if (!wait_q(s + 2) || !mbar_wait(&bars[C_PV_DONE + w], k & 1, p.status, &abort_flag)) break;
         tc_fence_after_sync();
-        issue_kq<D>(tmem + w * 128, sK, qbuf(s + 2));
+        issue_kq<D>(tmem + w * 128, k_kmaj, sdesc_sw128(qbuf(s + 2), 16, 1024));
         umma_commit(&bars[C_S_FULL + w]);
       }
     }

@@ -215,19 +215,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
     bool ok = mbar_wait(&bars[B_Q_FULL], 0, p.status, &abort_flag);
+    const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);  // Q as K-major A
     auto issue_pv = [&](int i) -> bool {
       const int c = i & 1;
       if (!mbar_wait(&bars[B_P_FULL + c], (i >> 1) & 1, p.status, &abort_flag)) return false;
       if (!mbar_wait(&bars[B_V_FULL + c], (i >> 1) & 1, p.status, &abort_flag)) return false;
       tc_fence_after_sync();
-      const uint32_t pa = sP + c * Lay::kPBytes;
-      const uint32_t vb = sV + c * Lay::kTileBytes;
+      const uint64_t pa = sdesc_sw128(sP + c * Lay::kPBytes, 16, 1024);               // P, K-major A
+      const uint64_t vb = sdesc_sw128(sV + c * Lay::kTileBytes, Lay::kBoxBytes, 1024);  // V, MN-major B
+      const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
-      for (int k = 0; k < kTile / 16; ++k) {
-        const uint64_t ad = sdesc_sw128(pa + (k >> 2) * Lay::kBoxBytes + (k & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(vb + k * 2048, Lay::kBoxBytes, 1024);
-        umma_bf16_ss(tmem + 256, ad, bd, idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
-      }
+      for (int k = 0; k < kTile / 16; ++k)
+        umma_bf16_ss(tmem + 256, sdesc_step(pa, (k >> 2) * Lay::kBoxBytes + (k & 3) * 32),
+                     sdesc_step(vb, k * 2048), idesc_pv, k > 0 ? 1u : acc0);
       umma_commit(&bars[B_P_EMPTY + c]);
       umma_commit(&bars[B_V_EMPTY + c]);
       return true;
@@ -238,12 +238,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && j >= 2) ok = mbar_wait(&bars[B_S_FREE + b], ((j - 2) >> 1) & 1, p.status, &abort_flag);
       if (!ok) break;
       tc_fence_after_sync();
-      const uint32_t kb = sK + b * Lay::kTileBytes;
+      const uint64_t k_desc = sdesc_sw128(sK + b * Lay::kTileBytes, 16, 1024);  // K, K-major B
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = (k >> 2) * Lay::kBoxBytes + (k & 3) * 32;
-        umma_bf16_ss(tmem + b * 128, sdesc_sw128(sQ + off, 16, 1024),
-                     sdesc_sw128(kb + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+        umma_bf16_ss(tmem + b * 128, sdesc_step(q_desc, off), sdesc_step(k_desc, off), idesc_s,
+                     k > 0 ? 1u : 0u);
       }
       umma_commit(&bars[B_S_FULL + b]);
       umma_commit(&bars[B_K_EMPTY + b]);

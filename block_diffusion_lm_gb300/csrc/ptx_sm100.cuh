@@ -232,6 +232,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Descriptor of the same operand `bytes` further on in shared memory: the
+// start address is the low 14-bit field (in 16-byte units) and every tile here
+// lies below 256 KB, so the add never carries out of it.  Building a base
+// descriptor once and stepping it this way keeps the single MMA-issuing
+// thread at a few instructions per MMA.
+__device__ __forceinline__ uint64_t sdesc_step(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
                                                       bool b_mn_major) {
