@@ -45,8 +45,7 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kHalf = 64;         // query columns per compute warpgroup
-constexpr int kStages = 2;        // Q and dO ring depth
-constexpr int kStageRows = 32;    // query rows per dQ reduce-add
+constexpr int kStages = 2;        // Q ring depth
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum BwdBar {
@@ -54,7 +53,7 @@ enum BwdBar {
   C_Q_FULL,                         // [kStages]
   C_Q_EMPTY = C_Q_FULL + kStages,   // [kStages]
   C_DO_FULL = C_Q_EMPTY + kStages,  // [kStages]
-  C_DO_EMPTY = C_DO_FULL + kStages,
+  C_DO_EMPTY = C_DO_FULL + kStages,  // [up to kStages]
   C_S_FULL = C_DO_EMPTY + kStages,
   C_DP_FULL,
   C_P_READY,
@@ -62,9 +61,10 @@ enum BwdBar {
   C_DS_READY,
   C_DQ_FULL,
   C_DQ_FREE,
-  C_STAGE_FULL,                     // [2] per half
-  C_STAGE_FREE = C_STAGE_FULL + 2,  // [2] per half
-  C_ACC_DONE = C_STAGE_FREE + 2,
+  C_STAGE_FULL,                     // [2] per half: dQ rows staged
+  C_X_FREE = C_STAGE_FULL + 2,      // [2] per half: dS^T box read by its reduce-add
+  C_SQ_FREE = C_X_FREE + 2,         // [2] per half: staging buffer read by its reduce-add
+  C_ACC_DONE = C_SQ_FREE + 2,
   C_DRAIN,
   C_COUNT
 };
@@ -74,16 +74,22 @@ struct BwdLayout {
   static constexpr int kTileBytes = kTile * D * 2;   // a 128-row bf16 tile (K, V, Q, dO)
   static constexpr int kBox = kTile * 128;           // one 64-column box of such a tile
   static constexpr int kXBox = kTile * kHalf * 2;    // dS^T box of one half (16 KB)
-  static constexpr int kStageBytes = kStageRows * D * 4;
-  static_assert(kStageBytes <= kXBox, "dQ staging must fit in a dS^T box");
+  // dQ rows of a half (64 x d fp32) are staged partly in its dS^T box, the
+  // rest in a buffer of its own; for d = 128 that buffer comes from keeping a
+  // single dO stage, whose refill has the dK, dQ^T and S^T MMAs to land.
+  static constexpr int kDOStages = (D == 128) ? 1 : 2;
+  static constexpr int kRowsX = kXBox / (D * 4);     // dQ rows staged in the dS^T box
+  static constexpr int kRowsSQ = kHalf - kRowsX;     // dQ rows staged in the own buffer
+  static_assert(kRowsX <= kHalf && kDOStages <= kStages, "staging split");
   static constexpr int kStatBytes = 2 * kTile * 4;   // LSE and D of one query tile
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kZero = kV + kTileBytes;      // zero K^T rows (d = 64 only)
   static constexpr int kQ = kZero + (D == 64 ? kBox : 0);
   static constexpr int kDO = kQ + kStages * kTileBytes;
-  static constexpr int kX = kDO + kStages * kTileBytes;
-  static constexpr int kStat = kX + 2 * kXBox;
+  static constexpr int kX = kDO + kDOStages * kTileBytes;
+  static constexpr int kSQ = kX + 2 * kXBox;          // [2 halves][kRowsSQ][D] fp32
+  static constexpr int kStat = kSQ + 2 * kRowsSQ * D * 4;
   static constexpr int kBar = kStat + kStages * kStatBytes;
   static constexpr int kMisc = kBar + C_COUNT * 8;   // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
@@ -94,31 +100,47 @@ struct BwdLayout {
   static constexpr uint32_t kColDK = 256 + D;
 };
 
-// Walk over (query head in group, segment, 128-row query tile) of a task.
+// Walk over the (query tile, segment, query head in group) steps of a task:
+// query tiles from the last down, every segment (query stream) that holds the
+// tile, then the heads of the GQA group.  Every key tile of a stream is read by
+// the last query tiles, so CTAs that start together stay on the same query
+// tile, and their dQ reduce-adds and Q / dO loads of that tile meet in L2.
 struct QWalk {
   const int32_t* seg0;
-  int n_segs, g, si, t, end, stream, flags;
-  __device__ void load_seg() {
-    const int32_t* s = seg0 + si * kSegWords;
-    stream = s[0];
-    t = s[1];
-    end = s[2];
-    flags = s[3];
+  int n_segs, G, g, si, t, stream, flags;
+  __device__ bool holds(int s, int tile) const {
+    const int32_t* x = seg0 + s * kSegWords;
+    return x[1] <= tile && tile < x[2];
   }
-  __device__ void start(const int32_t* s, int n) {
+  __device__ int find(int from) const {  // first segment >= from holding t
+    int s = from;
+    while (s < n_segs && !holds(s, t)) ++s;
+    return s;
+  }
+  __device__ void load_seg() {
+    const int32_t* x = seg0 + si * kSegWords;
+    stream = x[0];
+    flags = x[3];
+  }
+  __device__ void start(const int32_t* s, int n, int group) {
     seg0 = s;
     n_segs = n;
+    G = group;
     g = 0;
-    si = 0;
-    if (n > 0) load_seg();
+    t = -1;
+    for (int k = 0; k < n; ++k) t = max(t, s[k * kSegWords + 2] - 1);
+    si = find(0);
+    if (si < n_segs) load_seg();
   }
   __device__ void next() {
-    if (++t < end) return;
-    if (++si >= n_segs) {
-      si = 0;
-      ++g;
+    if (++g < G) return;
+    g = 0;
+    si = find(si + 1);
+    while (si >= n_segs && t > 0) {
+      --t;
+      si = find(0);
     }
-    load_seg();
+    if (si < n_segs) load_seg();
   }
 };
 
@@ -231,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   k_tile * kTile, bz);
     }
     QWalk w;
-    w.start(segs, n_segs);
+    w.start(segs, n_segs, p.G);
     int nq = 0;
     bool ok = true;
     for (int i = 0; i < n_steps && ok; ++i, w.next()) {
@@ -262,15 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (n_steps > 0 && warp == 2 && lane == 0) {
     // ===================== TMA producer: dO per step
     QWalk w;
-    w.start(segs, n_segs);
+    w.start(segs, n_segs, p.G);
     int ndo = 0;
     bool ok = true;
     for (int i = 0; i < n_steps && ok; ++i, w.next()) {
       const int h = kvh * p.G + w.g;
       const void* td = w.stream ? static_cast<const void*>(&tm_do1) : static_cast<const void*>(&tm_do0);
-      const int st = i % kStages;
-      if (i >= kStages)
-        ok = mbar_wait(&bars[C_DO_EMPTY + st], ((i / kStages) - 1) & 1, p.status, abort_flag);
+      const int st = i % Lay::kDOStages;
+      if (i >= Lay::kDOStages)
+        ok = mbar_wait(&bars[C_DO_EMPTY + st], ((i / Lay::kDOStages) - 1) & 1, p.status, abort_flag);
       if (!ok) break;
       mbar_arrive_expect_tx(&bars[C_DO_FULL + st], Lay::kTileBytes);
 #pragma unroll
@@ -280,8 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ndo = i + 1;
     }
     if (!ok) {
-      for (int i = (ndo > kStages ? ndo - kStages : 0); i < ndo; ++i)
-        mbar_wait(&bars[C_DO_FULL + i % kStages], (i / kStages) & 1, nullptr, nullptr, 200000000ull);
+      for (int i = (ndo > Lay::kDOStages ? ndo - Lay::kDOStages : 0); i < ndo; ++i)
+        mbar_wait(&bars[C_DO_FULL + i % Lay::kDOStages], (i / Lay::kDOStages) & 1, nullptr, nullptr,
+                  200000000ull);
     }
   } else if (n_steps > 0 && warp == 1 && lane == 0) {
     // ===================== MMA issuer
@@ -291,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return mbar_wait(&bars[C_Q_FULL + i % kStages], (i / kStages) & 1, p.status, abort_flag);
     };
     auto wait_do = [&](int i) {
-      return mbar_wait(&bars[C_DO_FULL + i % kStages], (i / kStages) & 1, p.status, abort_flag);
+      return mbar_wait(&bars[C_DO_FULL + i % Lay::kDOStages], (i / Lay::kDOStages) & 1, p.status,
+                       abort_flag);
     };
     const uint64_t k_kmaj = sdesc_sw128(sK, 16, 1024);   // K as K-major A (S^T)
     const uint64_t v_kmaj = sdesc_sw128(sV, 16, 1024);   // V as K-major A (dP^T)
@@ -310,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < n_steps && ok; ++i) {
       const int st = i % kStages;
       const uint32_t q_s = sQ + st * Lay::kTileBytes;
-      const uint32_t do_s = sDO + st * Lay::kTileBytes;
+      const uint32_t do_s = sDO + (i % Lay::kDOStages) * Lay::kTileBytes;
       const uint32_t acc0 = i > 0 ? 1u : 0u;
       // ---- dV += P^T dO, P^T in TMEM: half h's 32 packed columns at 64h
       if (!mbar_wait(&bars[C_P_READY], i & 1, p.status, abort_flag)) break;
@@ -323,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        sdesc_step(b, kk * 2048), idesc_kd, kk > 0 ? 1u : acc0);
       }
       umma_commit(&bars[C_PV_DONE]);
-      umma_commit(&bars[C_DO_EMPTY + st]);
+      umma_commit(&bars[C_DO_EMPTY + i % Lay::kDOStages]);
       // ---- dK += dS^T Q; dQ^T = K^T dS^T
       if (!mbar_wait(&bars[C_DS_READY], i & 1, p.status, abort_flag)) break;
       tc_fence_after_sync();
@@ -351,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars[C_DQ_FREE], i & 1, p.status, abort_flag) || !wait_do(i + 1)) break;
         tc_fence_after_sync();
         issue_kq<D>(tmem + Lay::kColDP, v_kmaj,
-                    sdesc_sw128(sDO + ((i + 1) % kStages) * Lay::kTileBytes, 16, 1024));
+                    sdesc_sw128(sDO + ((i + 1) % Lay::kDOStages) * Lay::kTileBytes, 16, 1024));
         umma_commit(&bars[C_DP_FULL]);
       }
     }
@@ -371,12 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kb = k_valid ? kpos / p.M : -1;
     const float sl2 = p.scale_log2;
     uint8_t* xbox = smem + Lay::kX + hf * Lay::kXBox;
-    float* stage = reinterpret_cast<float*>(xbox);  // dQ staging reuses this half's dS^T box
+    // dQ rows [0, kRowsX) of the half are staged in its dS^T box, the rest in
+    // its own buffer, both as [row][d] fp32
+    float* stage_x = reinterpret_cast<float*>(xbox);
+    float* stage_sq = reinterpret_cast<float*>(smem + Lay::kSQ) + hf * Lay::kRowsSQ * D;
     const bool k_ragged = (k_tile + 1) * kTile > p.L;
     QWalk wk;
-    wk.start(segs, n_segs);
+    wk.start(segs, n_segs, p.G);
     bool ok = true;
-    int uses = 0;  // staging uses of this half
     for (int i = 0; i < n_steps; ++i, wk.next()) {
       const int qs = wk.stream;
       const int h = kvh * p.G + wk.g;
@@ -419,11 +445,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C_P_READY]);
-      // ---- dS^T = P^T o (dP^T - D) into this half's box, once the previous
-      //      reduce-add has finished reading the box
+      // ---- dS^T = P^T o (dP^T - D) into this half's box, once the reduce-add
+      //      of the dQ rows staged there in the previous step has read them
+      //      (it was left in flight over the P^T work; the one of the own
+      //      buffer, issued after it, may still be)
+      if (i > 0 && leader && lane == 0) {
+        if (Lay::kRowsSQ > 0)
+          bulk_wait_group_read<1>();
+        else
+          bulk_wait_group_read<0>();
+        mbar_arrive(&bars[C_X_FREE + hf]);
+      }
       if (!mbar_wait_warp(&bars[C_DP_FULL], i & 1, p.status, abort_flag) ||
-          (uses > 0 &&
-           !mbar_wait_warp(&bars[C_STAGE_FREE + hf], (uses - 1) & 1, p.status, abort_flag))) {
+          (i > 0 && !mbar_wait_warp(&bars[C_X_FREE + hf], (i - 1) & 1, p.status, abort_flag))) {
         ok = false;
         break;
       }
@@ -458,39 +492,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C_DQ_FREE]);
-      // stage 32 query rows at a time ([row][d] fp32, in this half's box, which
-      // the completed dK / dQ^T MMAs no longer read) and reduce-add them
+      // stage the half's 64 dQ rows: the first kRowsX in its dS^T box, which
+      // the completed dK / dQ^T MMAs no longer read, the rest in its own
+      // buffer once the previous step's reduce-add from there has read it
+      if (r < D) {
 #pragma unroll
-      for (int part = 0; part < kHalf / kStageRows; ++part, ++uses) {
-        if (part > 0 &&
-            !mbar_wait_warp(&bars[C_STAGE_FREE + hf], (uses - 1) & 1, p.status, abort_flag)) {
+        for (int c = 0; c < Lay::kRowsX; ++c) stage_x[c * D + r] = dq[c];
+      }
+      if (Lay::kRowsSQ > 0) {
+        if (i > 0 && leader && lane == 0) {
+          bulk_wait_group_read<0>();
+          mbar_arrive(&bars[C_SQ_FREE + hf]);
+        }
+        if (i > 0 && !mbar_wait_warp(&bars[C_SQ_FREE + hf], (i - 1) & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
         if (r < D) {
 #pragma unroll
-          for (int c = 0; c < kStageRows; ++c) stage[c * D + r] = dq[part * kStageRows + c];
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[C_STAGE_FULL + hf]);
-        if (leader) {
-          if (!mbar_wait_warp(&bars[C_STAGE_FULL + hf], uses & 1, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            if (q0 + part * kStageRows < p.L) {  // rows past L (ragged last tile) are dropped
-              tma_reduce_add_3d(&tm_dqacc, stage, h * D, q0 + part * kStageRows, qs * p.batch + bz);
-              bulk_commit_group();
-              bulk_wait_group_read<0>();
-            }
-            mbar_arrive(&bars[C_STAGE_FREE + hf]);
-          }
-          __syncwarp();
+          for (int c = 0; c < Lay::kRowsSQ; ++c) stage_sq[c * D + r] = dq[Lay::kRowsX + c];
         }
       }
-      if (!ok) break;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C_STAGE_FULL + hf]);
+      if (leader) {
+        if (!mbar_wait_warp(&bars[C_STAGE_FULL + hf], i & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        // one bulk group per buffer, the dS^T box first (its rows are needed
+        // back soonest); rows past L (ragged last tile) are dropped, leaving
+        // an empty group
+        if (lane == 0) {
+          const int plane = qs * p.batch + bz;
+          if (q0 < p.L) tma_reduce_add_3d(&tm_dqacc, stage_x, h * D, q0, plane);
+          bulk_commit_group();
+          if (Lay::kRowsSQ > 0) {
+            if (q0 + Lay::kRowsX < p.L)
+              tma_reduce_add_3d(&tm_dqacc, stage_sq, h * D, q0 + Lay::kRowsX, plane);
+            bulk_commit_group();
+          }
+        }
+        __syncwarp();
+      }
     }
     if (leader && lane == 0) bulk_wait_group<0>();  // reduce-adds complete before exit
     // ---- epilogue (half 0): dV, dK rows of this key tile
@@ -563,8 +608,8 @@ static cudaError_t launch_bwd_d(const CUtensorMap* maps, const BwdParams& p, int
 
 // Rows of one TMA box for the query-side maps (Q, dO) and the LSE/D maps.
 int bwd_query_box_rows() { return kTile; }
-// Query rows of one dQ reduce-add box.
-int bwd_dq_box_rows() { return kStageRows; }
+// Query rows of one dQ reduce-add box: a 16 KB fp32 box of d columns.
+int bwd_dq_box_rows(int d) { return (kTile * kHalf * 2) / (d * 4); }
 
 // maps: q_clean, q_corr, k_clean, k_corr, v_clean, v_corr, do_clean, do_corr
 //       (128-row boxes), lse ({L, batch*2*Hq} fp32) and dsum ({L, 2*batch*Hq}

@@ -18,7 +18,7 @@ cudaError_t launch_fwd(int d, const CUtensorMap* maps, const FwdParams& p, int n
 cudaError_t launch_bwd(int d, const CUtensorMap* maps, const BwdParams& p, int n_tasks,
                        cudaStream_t stream);
 int bwd_query_box_rows();
-int bwd_dq_box_rows();
+int bwd_dq_box_rows(int d);
 cudaError_t launch_lse_merge(const MergeArgs& a, int n_parts, int64_t rows, int Hq, int d,
                              void* o_out, float* z_out, cudaStream_t stream);
 cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, float* Dsum, float* dq_acc,
@@ -288,7 +288,7 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
   const void* dc = do_clean ? do_clean : do_corr;
   const int qbox = bwd_query_box_rows();
   if (!make_map_dqacc(&maps[10], dq_acc, p.Hq, p.d, p.L, 2 * static_cast<int64_t>(p.batch),
-                      bwd_dq_box_rows()))
+                      bwd_dq_box_rows(p.d)))
     return CSBP_ERR_CUDA;
   if (!make_map(&maps[0], qc, p.Hq, p.d, p.L, p.batch, qbox) ||
       !make_map(&maps[1], in->q_corr, p.Hq, p.d, p.L, p.batch, qbox) ||
