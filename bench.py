@@ -19,6 +19,7 @@ workload on its own GPU (no collective on the data path): weak scaling.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -49,6 +50,40 @@ def parse():
     ap.add_argument("--L", type=int, default=None,
                     help="override the sequence length (profiling captures of a smaller case)")
     return ap.parse_args()
+
+
+# Sources that determine bwd_kernel's machine code; a DRAM-traffic figure
+# counts only while their hash matches the one recorded with it.
+BWD_KERNEL_SOURCES = ("attn_bwd.cu", "ptx_sm100.cuh", "csbp_internal.h")
+
+
+def bwd_kernel_source_hash():
+    h = hashlib.sha256()
+    for name in BWD_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "block_diffusion_lm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload):
+    """DRAM bytes (read + write) per bwd_kernel launch from the committed ncu
+    summary of this workload, or None if there is none or the kernel changed
+    since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"bwd_kernel_{workload}_dram.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip().strip("`- ")] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256") != bwd_kernel_source_hash():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def peaks():
@@ -251,6 +286,7 @@ def main():
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)
+    csbp.kernel_timing(True)
     start_all = torch.cuda.Event(enable_timing=True)
     end_all = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -264,6 +300,8 @@ def main():
         end_all.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
+    csbp.kernel_timing(False)
+    fwd_k_ms, n_fwd_k, bwd_k_ms, n_bwd_k = csbp.kernel_timing_read()
     attn.check(stream)
     total_ms = start_all.elapsed_time(end_all)
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
@@ -284,7 +322,10 @@ def main():
     pk = peaks()
     bwd_avg = statistics.mean(bwd_ms)
     fwd_avg = statistics.mean(fwd_ms)
-    achieved = w.useful_bwd_flops() / (bwd_avg * 1e-3) / 1e12
+    bwd_call_tflops = w.useful_bwd_flops() / (bwd_avg * 1e-3) / 1e12
+    bwd_kernel_ms = bwd_k_ms / max(n_bwd_k, 1)      # main kernel alone, CUDA events
+    fwd_kernel_ms = fwd_k_ms / max(n_fwd_k, 1)
+    achieved = w.useful_bwd_flops() / (bwd_kernel_ms * 1e-3) / 1e12
     peak = pk["bf16_sustained"]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -296,12 +337,14 @@ def main():
         "pct_of_bf16_peak": value / world / pk["bf16_sustained"],
         "fwd_ms": fwd_avg, "bwd_ms": bwd_avg,
         "fwd_tflops": w.useful_fwd_flops() / (fwd_avg * 1e-3) / 1e12,
-        "bwd_tflops": achieved,
-        "roofline": {"bound": "tensor", "kernel": f"bwd_kernel<{w.d}> (csbp_attn_bwd call)",
+        "bwd_tflops": bwd_call_tflops,
+        "fwd_kernel_ms": fwd_kernel_ms, "bwd_kernel_ms": bwd_kernel_ms,
+        "roofline": {"bound": "tensor", "kernel": f"bwd_kernel<{w.d}>",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "peak_source": f"bf16_tflops_sustained of {pk['source']}",
-                     "traffic": None},
+                     "launch_ms": bwd_kernel_ms, "launches_timed": n_bwd_k,
+                     "traffic": recorded_traffic(w.name)},
         "e2e": e2e,
         "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clocks,

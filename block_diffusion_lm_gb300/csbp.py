@@ -20,7 +20,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "csbp.h")
 OK = 0
 STATUS = {0: "CSBP_OK", -1: "CSBP_ERR_INVALID", -2: "CSBP_ERR_UNSUPPORTED",
           -3: "CSBP_ERR_WORKSPACE", -4: "CSBP_ERR_CUDA", -5: "CSBP_ERR_TIMEOUT",
-          -6: "CSBP_ERR_CAPACITY"}
+          -6: "CSBP_ERR_CAPACITY", -7: "CSBP_ERR_DEVICE"}
 
 
 class CsbpError(RuntimeError):
@@ -74,8 +74,11 @@ def lib():
         L.csbp_status_string.argtypes = [ctypes.c_int]
         L.csbp_status_string.restype = ctypes.c_char_p
         L.csbp_version.restype = i32
+        L.csbp_kernel_timing.argtypes = [i32]
+        L.csbp_kernel_timing_read.argtypes = [P(ctypes.c_double), P(i32), P(ctypes.c_double),
+                                              P(i32)]
         for fn in ("csbp_block_schedule", "csbp_attn_fwd", "csbp_attn_bwd", "csbp_lse_merge",
-                   "csbp_check_status"):
+                   "csbp_check_status", "csbp_kernel_timing", "csbp_kernel_timing_read"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -119,6 +122,21 @@ def block_schedule(problem: Problem):
                                    ctypes.byref(info))
     _check("csbp_block_schedule", st)
     return bo[:B], co[:2 * problem.P], words, info
+
+
+def kernel_timing(enable: bool) -> None:
+    """Start (clearing the record) or stop event timing of the main kernels."""
+    _check("csbp_kernel_timing", lib().csbp_kernel_timing(1 if enable else 0))
+
+
+def kernel_timing_read():
+    """(fwd_kernel_ms, n_fwd, bwd_kernel_ms, n_bwd) summed over the record."""
+    fm, bm = ctypes.c_double(), ctypes.c_double()
+    fn, bn = ctypes.c_int32(), ctypes.c_int32()
+    _check("csbp_kernel_timing_read",
+           lib().csbp_kernel_timing_read(ctypes.byref(fm), ctypes.byref(fn), ctypes.byref(bm),
+                                         ctypes.byref(bn)))
+    return fm.value, fn.value, bm.value, bn.value
 
 
 def workspace_bytes(problem: Problem, which: int) -> int:

@@ -7,6 +7,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "csbp.h"
 #include "csbp_internal.h"
@@ -151,11 +152,92 @@ WorkOffsets work_offsets(const csbp_schedule_info* info) {
   return o;
 }
 
+// ---------------------------------------------------------------- timing
+// Event pairs around the main kernels, for csbp_kernel_timing(_read).
+struct KernelTimer {
+  static constexpr int kCap = 4096;
+  std::mutex mu;
+  bool on = false;
+  int device = -1;
+  std::vector<cudaEvent_t> start, stop;
+  std::vector<int> kind;  // 0 fwd, 1 bwd, per recorded pair
+};
+KernelTimer& timer() {
+  static KernelTimer t;
+  return t;
+}
+
+// Returns the pair index to record, or -1.
+int timer_begin(int kind, cudaStream_t stream) {
+  KernelTimer& t = timer();
+  std::lock_guard<std::mutex> lk(t.mu);
+  if (!t.on || static_cast<int>(t.kind.size()) >= KernelTimer::kCap) return -1;
+  const int i = static_cast<int>(t.kind.size());
+  if (cudaEventRecord(t.start[i], stream) != cudaSuccess) return -1;
+  t.kind.push_back(kind);
+  return i;
+}
+
+void timer_end(int i, cudaStream_t stream) {
+  if (i < 0) return;
+  KernelTimer& t = timer();
+  std::lock_guard<std::mutex> lk(t.mu);
+  cudaEventRecord(t.stop[i], stream);
+}
+
 }  // namespace
 
 }  // namespace csbp
 
 using namespace csbp;
+
+extern "C" csbp_status csbp_kernel_timing(int32_t enable) {
+  KernelTimer& t = timer();
+  std::lock_guard<std::mutex> lk(t.mu);
+  if (!enable) {
+    t.on = false;
+    return CSBP_OK;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSBP_ERR_CUDA;
+  if (t.device != dev) {
+    for (auto e : t.start) cudaEventDestroy(e);
+    for (auto e : t.stop) cudaEventDestroy(e);
+    t.start.assign(KernelTimer::kCap, nullptr);
+    t.stop.assign(KernelTimer::kCap, nullptr);
+    for (int i = 0; i < KernelTimer::kCap; ++i) {
+      if (cudaEventCreate(&t.start[i]) != cudaSuccess || cudaEventCreate(&t.stop[i]) != cudaSuccess) {
+        t.device = -1;
+        return CSBP_ERR_CUDA;
+      }
+    }
+    t.device = dev;
+  }
+  t.kind.clear();
+  t.on = true;
+  return CSBP_OK;
+}
+
+extern "C" csbp_status csbp_kernel_timing_read(double* fwd_ms, int32_t* n_fwd, double* bwd_ms,
+                                               int32_t* n_bwd) {
+  KernelTimer& t = timer();
+  std::lock_guard<std::mutex> lk(t.mu);
+  double ms[2] = {0.0, 0.0};
+  int32_t n[2] = {0, 0};
+  for (size_t i = 0; i < t.kind.size(); ++i) {
+    float e = 0.f;
+    if (cudaEventSynchronize(t.stop[i]) != cudaSuccess ||
+        cudaEventElapsedTime(&e, t.start[i], t.stop[i]) != cudaSuccess)
+      return CSBP_ERR_CUDA;
+    ms[t.kind[i]] += e;
+    n[t.kind[i]] += 1;
+  }
+  if (fwd_ms) *fwd_ms = ms[0];
+  if (n_fwd) *n_fwd = n[0];
+  if (bwd_ms) *bwd_ms = ms[1];
+  if (n_bwd) *n_bwd = n[1];
+  return CSBP_OK;
+}
 
 extern "C" int32_t csbp_version(void) { return 100; }
 
@@ -168,6 +250,7 @@ extern "C" const char* csbp_status_string(csbp_status s) {
     case CSBP_ERR_CUDA: return "CUDA error";
     case CSBP_ERR_TIMEOUT: return "device wait timed out";
     case CSBP_ERR_CAPACITY: return "output buffer too small";
+    case CSBP_ERR_DEVICE: return "kernel refused its launch environment";
   }
   return "unknown status";
 }
@@ -230,7 +313,10 @@ extern "C" csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inp
     const int64_t n_lse = static_cast<int64_t>(p.P + 1) * 2 * p.batch * p.Hq * p.L;
     if (launch_fill(fp.part_lse, n_lse, -INFINITY, stream) != cudaSuccess) return CSBP_ERR_CUDA;
   }
-  if (launch_fwd(p.d, maps, fp, info->n_fwd_tasks, stream) != cudaSuccess) return CSBP_ERR_CUDA;
+  const int timed = timer_begin(0, stream);
+  const cudaError_t fe = launch_fwd(p.d, maps, fp, info->n_fwd_tasks, stream);
+  timer_end(timed, stream);
+  if (fe != cudaSuccess) return CSBP_ERR_CUDA;
   if (p.P > 1) {
     const int n_parts = p.P + 1;
     const int64_t slab_o = static_cast<int64_t>(p.L) * p.Hq * p.d;
@@ -331,7 +417,10 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
   bp.dv[0] = dv_clean;
   bp.dv[1] = dv_corr;
   bp.status = reinterpret_cast<int*>(ws + wl.status);
-  if (launch_bwd(p.d, maps, bp, info->n_bwd_tasks, stream) != cudaSuccess) return CSBP_ERR_CUDA;
+  const int timed = timer_begin(1, stream);
+  const cudaError_t be = launch_bwd(p.d, maps, bp, info->n_bwd_tasks, stream);
+  timer_end(timed, stream);
+  if (be != cudaSuccess) return CSBP_ERR_CUDA;
 
   void* dq_s[2] = {dq_clean, dq_corr};
   for (int qs = hc ? 0 : 1; qs < 2; ++qs) {
@@ -370,7 +459,7 @@ extern "C" csbp_status csbp_check_status(void* workspace, void* stream) {
     return CSBP_ERR_CUDA;
   if (v != 0) {
     if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return CSBP_ERR_CUDA;
-    return CSBP_ERR_TIMEOUT;
+    return v == 1 ? CSBP_ERR_TIMEOUT : CSBP_ERR_DEVICE;  // device codes: 1 timeout, 2 misaligned
   }
   return CSBP_OK;
 }

@@ -56,7 +56,9 @@ typedef enum {
   CSBP_ERR_WORKSPACE = -3,   /* workspace smaller than csbp_workspace_bytes  */
   CSBP_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed            */
   CSBP_ERR_TIMEOUT = -5,     /* a bounded device wait gave up                */
-  CSBP_ERR_CAPACITY = -6     /* output buffer too small; size reported       */
+  CSBP_ERR_CAPACITY = -6,    /* output buffer too small; size reported       */
+  CSBP_ERR_DEVICE = -7       /* a kernel refused its launch environment
+                                (shared-memory window not 1024-byte aligned) */
 } csbp_status;
 
 /* Problem description.
@@ -206,8 +208,23 @@ csbp_status csbp_lse_merge(int32_t n_parts, const float* const* o_parts,
 
 /* Synchronise `stream`, then read and clear the device status word kept at
  * the start of `workspace` by csbp_attn_fwd / csbp_attn_bwd.  Returns
- * CSBP_ERR_TIMEOUT if a bounded device wait gave up since the last check. */
+ * CSBP_ERR_TIMEOUT if a bounded device wait gave up since the last check,
+ * CSBP_ERR_DEVICE if a kernel refused to run (its shared-memory window was
+ * not 1024-byte aligned; it then wrote nothing). */
 csbp_status csbp_check_status(void* workspace, void* stream);
+
+/* Kernel timing, a profiling aid with no counterpart in the method; off by
+ * default.  csbp_kernel_timing(1) creates a pool of CUDA events on the
+ * current device and clears the record; while it is on, every csbp_attn_fwd
+ * and csbp_attn_bwd call records an event pair on its stream around its main
+ * kernel (fwd_kernel / bwd_kernel), up to 4096 pairs in all (later calls are
+ * not timed).  csbp_kernel_timing(0) stops recording and keeps the record.
+ * csbp_kernel_timing_read synchronises the recorded events and returns the
+ * summed device milliseconds and launch counts of each kind (any output
+ * pointer may be NULL).  CSBP_ERR_CUDA if an event call fails. */
+csbp_status csbp_kernel_timing(int32_t enable);
+csbp_status csbp_kernel_timing_read(double* fwd_ms, int32_t* n_fwd, double* bwd_ms,
+                                    int32_t* n_bwd);
 
 /* Human-readable name of a status code (static string). */
 const char* csbp_status_string(csbp_status status);

@@ -111,6 +111,25 @@ def test_repeat_calls_are_deterministic_in_forward():
     assert torch.equal(a[1], b[1]) and torch.equal(a[0], b[0]) and torch.equal(a[2], b[2])
 
 
+def test_kernel_timing_records_one_pair_per_call():
+    w = Workload("timing", 1, 512, 32, 2, 1, 128, seed=33)
+    t = make_inputs(w, "cuda")
+    attn = csbp.BlockDiffusionAttention(1, 512, 32, 2, 1, 128)
+    out = attn.forward(t)
+    attn.backward(t, out)
+    torch.cuda.synchronize()
+    csbp.kernel_timing(True)
+    for _ in range(3):
+        out = attn.forward(t, out=out)
+        attn.backward(t, out)
+    csbp.kernel_timing(False)
+    attn.forward(t, out=out)  # not recorded
+    fwd_ms, n_fwd, bwd_ms, n_bwd = csbp.kernel_timing_read()
+    assert (n_fwd, n_bwd) == (3, 3)
+    assert fwd_ms > 0.0 and bwd_ms > 0.0
+    attn.check()
+
+
 # ------------------------------------------------------------------ full size
 def _invariants(w, t, g):
     """sum_j dK_j = 0 per KV head; sum_j dV_j = sum of the group's dO rows."""
