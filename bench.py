@@ -358,36 +358,65 @@ def main():
 
 
 def run_e2e(args, w, t, attn, out, grads, stream, dev, world, flops, in_bytes):
-    """Same step through the public API from pinned host inputs, with the
-    outputs and gradients copied back, all inside the timed region."""
+    """Same steps through the public API from pinned host inputs, with the
+    outputs and gradients copied back, all inside the timed region.  Copies
+    run on their own streams with two buffer sets, so step i+1's inputs go
+    up and step i's results come down while step i computes; the region runs
+    from the first input copy to the last result copy."""
     import torch
     import torch.distributed as dist
 
     host_in = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in t.items()}
-    dev_in = {k: (torch.empty_like(v) if v is not None else None) for k, v in t.items()}
-    res = [x for x in (*out, *grads.values()) if x is not None]
-    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in res]
-    out_bytes = sum(x.numel() * x.element_size() for x in res)
+    sets = []
+    for k in range(2):
+        o = out if k == 0 else attn.alloc_outputs()
+        g = grads if k == 0 else attn.alloc_grads()
+        d_in = {n: (torch.empty_like(v) if v is not None else None) for n, v in t.items()}
+        res = [x for x in (*o, *g.values()) if x is not None]
+        h_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in res]
+        sets.append((d_in, o, g, res, h_out))
+    out_bytes = sum(x.numel() * x.element_size() for x in sets[0][3])
     e2e_steps = max(3, min(args.steps, 10))
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=False)
+    in_ready = [ev(), ev()]
+    done = [ev(), ev()]
+    read = [ev(), ev()]
+    for e in done + read:
+        e.record(stream)
 
-    def e2e_step():
-        for k, v in host_in.items():
-            if v is not None:
-                dev_in[k].copy_(v, non_blocking=True)
-        attn.forward(dev_in, out=out, stream=stream)
-        attn.backward(dev_in, out, grads=grads, stream=stream)
-        for hsrc, hdst in zip(res, host_out):
-            hdst.copy_(hsrc, non_blocking=True)
+    def run(n, e_start=None, e_end=None):
+        for i in range(n):
+            k = i % 2
+            d_in, o, g, res, h_out = sets[k]
+            with torch.cuda.stream(up):
+                up.wait_event(done[k])          # the step that last read these inputs
+                if i == 0 and e_start is not None:
+                    e_start.record(up)
+                for name, v in host_in.items():
+                    if v is not None:
+                        d_in[name].copy_(v, non_blocking=True)
+                in_ready[k].record(up)
+            stream.wait_event(in_ready[k])
+            stream.wait_event(read[k])          # its outputs were copied down
+            attn.forward(d_in, out=o, stream=stream)
+            attn.backward(d_in, o, grads=g, stream=stream)
+            done[k].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(done[k])
+                for hsrc, hdst in zip(res, h_out):
+                    hdst.copy_(hsrc, non_blocking=True)
+                read[k].record(down)
+        if e_end is not None:
+            with torch.cuda.stream(down):
+                e_end.record(down)
 
-    with torch.cuda.stream(stream):
-        e2e_step()
-        torch.cuda.synchronize(dev)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
+    run(2)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    run(e2e_steps, e0, e1)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if world > 1:
@@ -396,7 +425,7 @@ def run_e2e(args, w, t, attn, out, grads, stream, dev, world, flops, in_bytes):
         e2e_ms = x.item()
     e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
     return {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": in_bytes,
-            "d2h_bytes_per_step": out_bytes}
+            "d2h_bytes_per_step": out_bytes, "overlap": "copies on separate streams, 2 buffer sets"}
 
 
 if __name__ == "__main__":
