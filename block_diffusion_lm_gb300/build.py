@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcsbp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["schedule.cpp", "csbp_api.cu", "attn_fwd.cu", "attn_fwd_pair.cu", "attn_bwd.cu", "elementwise.cu",
+SOURCES = ["schedule.cpp", "csbp_api.cu", "attn_fwd.cu", "attn_bwd.cu", "elementwise.cu",
            "noalloc.cu"]
 
 

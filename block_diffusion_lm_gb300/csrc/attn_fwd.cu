@@ -8,18 +8,28 @@
 // normalised fp32 partial per key part for the exact LSE merge of the
 // section "在线 softmax 合并：为什么分两段算仍是同一个注意力".
 //
-// One CTA owns one 128-row query tile of one (batch, query head) and walks
-// the key-tile segments of its work-list task.  Roles (256 threads):
-//   warp 0 lane 0  TMA producer: Q once, then K_j / V_j into 2-stage rings
-//   warp 1 lane 0  MMA issuer:   S_j = Q K_j^T into TMEM (double buffered),
-//                                O += P_{j-1} V_{j-1} into TMEM
-//   warps 4..7     softmax: thread t owns query row t (TMEM lane t); reads
-//                  S_j with tcgen05.ld, masks partial tiles, keeps a running
-//                  reference max, writes P_j (bf16) to shared memory in the
-//                  128B-swizzled K-major layout the PV MMA reads, and
-//                  rescales the TMEM accumulator only when the row max grows
-//                  by more than 2^8 (exact: O and l share the reference).
-// TMEM columns: S buffers at 0 and 128, O at 256 (512 allocated).
+// One CTA owns two consecutive work-list tasks of one (batch, query head):
+// two 128-row query tiles ("slots").  The list is sorted heaviest first, and
+// equal-cost tasks of one key part and query copy are adjacent, so the two
+// usually read the same key tiles.  It walks the union of their key tiles in (copy,
+// tile) order, so a key tile both slots read is loaded once.  Each slot has
+// its own softmax warpgroup, and the two keep the tensor pipe busy in turn:
+// while one slot's softmax runs, the other slot's MMAs do.  Roles (384
+// threads):
+//   warp 0 lane 0  TMA producer: both Q tiles once, then K / V of each key
+//                  tile of the union into 2-stage rings
+//   warp 1 lane 0  MMA issuer, per key tile of the union and slot by slot:
+//                  O_s += P_s V of the previous tile, then S_s = Q_s K^T of
+//                  this one (once that PV has read the P_s it overwrites)
+//   warps 4..7, 8..11  softmax of slot 0, 1: thread t owns query row t (TMEM
+//                  lane t); reads S with tcgen05.ld, masks partial tiles,
+//                  keeps a running reference max, writes P (bf16 pairs) back
+//                  over the first 64 columns of its S, which the PV MMA reads
+//                  as its A operand, and rescales the TMEM accumulator only
+//                  when the row max grows by more than 2^8 (exact: O and l
+//                  share the reference).
+// TMEM columns: S of slot s at 128 s, O of slot s at 256 + d s.  All shared
+// state lives in the dynamic window, which must start 1024-byte aligned.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -30,60 +40,86 @@ namespace csbp {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Per-warpgroup register budgets (setmaxnreg): producer / MMA, softmax.
+// Their sum must not exceed the launch allocation (checked on the host).
+constexpr uint32_t kRegsLow = 112;
+constexpr uint32_t kRegsSoftmax = 192;
+constexpr int kRegsNeeded = 128 * kRegsLow + 256 * kRegsSoftmax;
+
+enum FwdBar {
+  B_Q_FULL = 0,               // [2] per slot
+  B_K_FULL = B_Q_FULL + 2,    // [2] ring stage
+  B_K_EMPTY = B_K_FULL + 2,   // [2]
+  B_V_FULL = B_K_EMPTY + 2,   // [2]
+  B_V_EMPTY = B_V_FULL + 2,   // [2]
+  B_S_FULL = B_V_EMPTY + 2,   // [2] per slot
+  B_P_FULL = B_S_FULL + 2,    // [2] per slot (its four softmax warps)
+  B_PV_DONE = B_P_FULL + 2,   // [2] per slot
+  B_DRAIN = B_PV_DONE + 2,
+  B_COUNT
+};
 
 template <int D>
 struct FwdLayout {
   static constexpr int kTileBytes = kTile * D * 2;     // Q/K/V tile (bf16)
   static constexpr int kBoxBytes = kTile * 64 * 2;     // one 64-column TMA box
-  static constexpr int kPBytes = kTile * kTile * 2;    // P tile (bf16)
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;           // 2 stages
+  static constexpr int kQ = 0;                         // 2 slots
+  static constexpr int kK = kQ + 2 * kTileBytes;       // 2 stages
   static constexpr int kV = kK + 2 * kTileBytes;       // 2 stages
-  static constexpr int kP = kV + 2 * kTileBytes;       // 2 buffers
-  static constexpr int kBytes = kP + 2 * kPBytes;
-  static constexpr int kDynSmem = kBytes + 1024;       // + alignment slack
+  static constexpr int kBar = kV + 2 * kTileBytes;
+  static constexpr int kMisc = kBar + B_COUNT * 8;     // tmem base, abort flag
+  static constexpr int kDynSmem = kMisc + 16;
+  static constexpr uint32_t kColO = 256;               // O of slot s at kColO + D s
 };
 
-enum FwdBar {
-  B_Q_FULL = 0,
-  B_K_FULL,            // [2]
-  B_V_FULL = B_K_FULL + 2,
-  B_K_EMPTY = B_V_FULL + 2,
-  B_V_EMPTY = B_K_EMPTY + 2,
-  B_S_FULL = B_V_EMPTY + 2,
-  B_S_FREE = B_S_FULL + 2,
-  B_P_FULL = B_S_FREE + 2,
-  B_P_EMPTY = B_P_FULL + 2,
-  B_DRAIN = B_P_EMPTY + 2,
-  B_COUNT
-};
-
-// Sequential walk over the key tiles of a task's segments.
-struct TileWalk {
+// Walk over the key tiles of one task's segments, in (copy, tile) order.
+struct SlotWalk {
   const int32_t* seg;
-  int remaining_segs;
+  int segs_left, left;  // segments after the current one, tiles not yet passed
   int stream, t, end, flags;
-  __device__ void start(const int32_t* s, int n) {
+  __device__ void start(const int32_t* s, int n_segs, int n_tiles) {
     seg = s;
-    remaining_segs = n;
-    end = 0;
-    t = 0;
-    advance_segment();
+    segs_left = n_segs;
+    left = n_tiles;
+    stream = t = end = flags = 0;
+    load();
   }
-  __device__ void advance_segment() {
-    if (remaining_segs <= 0) return;
+  __device__ void load() {
+    if (segs_left <= 0) return;
     stream = seg[0];
     t = seg[1];
     end = seg[2];
     flags = seg[3];
     seg += kSegWords;
-    --remaining_segs;
+    --segs_left;
   }
+  __device__ int key() const { return left > 0 ? (stream << 24) + t : 0x7fffffff; }
   __device__ void next() {
-    ++t;
-    if (t >= end) advance_segment();
+    --left;
+    if (++t >= end) load();
+  }
+};
+
+// Walk over the union of two slots' key tiles: which slots read the current
+// tile, and its copy and index.
+struct PairWalk {
+  SlotWalk w[2];
+  int in0, in1, stream, t;
+  __device__ void settle() {
+    const int k0 = w[0].key(), k1 = w[1].key();
+    const int k = min(k0, k1);
+    in0 = (k0 == k) && k != 0x7fffffff;
+    in1 = (k1 == k) && k != 0x7fffffff;
+    stream = in0 ? w[0].stream : w[1].stream;
+    t = in0 ? w[0].t : w[1].t;
+  }
+  __device__ bool valid() const { return in0 || in1; }
+  __device__ void next() {
+    if (in0) w[0].next();
+    if (in1) w[1].next();
+    settle();
   }
 };
 
@@ -114,285 +150,315 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q0, const __grid_constant__ CUtensorMap tm_q1,
                const __grid_constant__ CUtensorMap tm_k0, const __grid_constant__ CUtensorMap tm_k1,
                const __grid_constant__ CUtensorMap tm_v0, const __grid_constant__ CUtensorMap tm_v1,
-               const FwdParams p) {
+               const FwdParams p, int n_tasks) {
   using Lay = FwdLayout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t bars[B_COUNT];
-  __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_flag;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // layout below needs a 1024-aligned window
+    if (threadIdx.x == 0) atomicExch(p.status, DEV_MISALIGNED);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + Lay::kMisc);
+  int* abort_flag = reinterpret_cast<int*>(smem + Lay::kMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- decode the unit: (task, batch, query head)
+  // ---- decode the unit: (task pair, batch, query head)
   const int hb = p.Hq * p.batch;
-  const int task = blockIdx.x / hb;
-  const int rem = blockIdx.x - task * hb;
+  const int pair = blockIdx.x / hb;
+  const int rem = blockIdx.x - pair * hb;
   const int bz = rem / p.Hq;
   const int h = rem - bz * p.Hq;
   const int kvh = h / p.G;
-  const int32_t* tw = p.tasks + static_cast<int64_t>(task) * kTaskWords;
-  const int q_stream = tw[0];
-  const int q_tile = tw[1];
-  const int part = tw[2];
-  const int32_t* segs = p.segs + static_cast<int64_t>(tw[3]) * kSegWords;
-  const int n_segs = tw[4];
-  const int n_tiles = tw[5];
+  const int n_slots = (2 * pair + 1 < n_tasks) ? 2 : 1;
+  auto task_words = [&](int s) { return p.tasks + static_cast<int64_t>(2 * pair + s) * kTaskWords; };
+  auto slot_walk = [&](int s, SlotWalk& w) {
+    if (s < n_slots) {
+      const int32_t* tw = task_words(s);
+      w.start(p.segs + static_cast<int64_t>(tw[3]) * kSegWords, tw[4], tw[5]);
+    } else {
+      w.start(nullptr, 0, 0);
+    }
+  };
+  auto slot_tiles = [&](int s) { return s < n_slots ? task_words(s)[5] : 0; };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < B_COUNT; ++i) {
-      const bool per_warp = (i >= B_S_FREE && i < B_S_FREE + 2) || (i >= B_P_FULL && i < B_P_FULL + 2);
-      mbar_init(&bars[i], per_warp ? 4 : 1);  // softmax warps arrive once each
-    }
-    abort_flag = 0;
+    for (int i = 0; i < B_COUNT; ++i)
+      mbar_init(&bars[i], (i >= B_P_FULL && i < B_P_FULL + 2) ? 4 : 1);
+    *abort_flag = 0;
     fence_mbarrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_sh, 512);
+    tmem_alloc(tmem_base_sh, 512);
     tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem = tmem_base_sh;
+  const uint32_t tmem = *tmem_base_sh;
 
-  const uint32_t sQ = smem_u32(smem + Lay::kQ);
-  const uint32_t sK = smem_u32(smem + Lay::kK);
-  const uint32_t sV = smem_u32(smem + Lay::kV);
-  const uint32_t sP = smem_u32(smem + Lay::kP);
-
-  if (warp == 0 && lane == 0) {
-    // ===================== TMA producer
-    const void* tq = q_stream ? static_cast<const void*>(&tm_q1) : static_cast<const void*>(&tm_q0);
-    prefetch_tmap(tq);
-    prefetch_tmap(&tm_k0);
-    prefetch_tmap(&tm_k1);
-    prefetch_tmap(&tm_v0);
-    prefetch_tmap(&tm_v1);
-    mbar_arrive_expect_tx(&bars[B_Q_FULL], Lay::kTileBytes);
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsLow>();
+    if (warp == 0 && lane == 0) {
+      // ===================== TMA producer
+      prefetch_tmap(&tm_q0);
+      prefetch_tmap(&tm_q1);
+      prefetch_tmap(&tm_k0);
+      prefetch_tmap(&tm_k1);
+      prefetch_tmap(&tm_v0);
+      prefetch_tmap(&tm_v1);
+      for (int s = 0; s < n_slots; ++s) {
+        const int32_t* tw = task_words(s);
+        const void* tq = tw[0] ? static_cast<const void*>(&tm_q1) : static_cast<const void*>(&tm_q0);
+        mbar_arrive_expect_tx(&bars[B_Q_FULL + s], Lay::kTileBytes);
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c)
-      tma_load_3d(smem + Lay::kQ + c * Lay::kBoxBytes, tq, &bars[B_Q_FULL], h * D + c * 64,
-                  q_tile * kTile, bz);
-    TileWalk w;
-    w.start(segs, n_segs);
-    int nk = 0, nv = 0;  // K / V tiles whose loads were issued
-    bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j, w.next()) {
-      const int b = j & 1;
-      const void* tk = w.stream ? static_cast<const void*>(&tm_k1) : static_cast<const void*>(&tm_k0);
-      const void* tv = w.stream ? static_cast<const void*>(&tm_v1) : static_cast<const void*>(&tm_v0);
-      if (j >= 2) ok = mbar_wait(&bars[B_K_EMPTY + b], ((j - 2) >> 1) & 1, p.status, &abort_flag);
-      if (!ok) break;
-      mbar_arrive_expect_tx(&bars[B_K_FULL + b], Lay::kTileBytes);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(smem + Lay::kK + b * Lay::kTileBytes + c * Lay::kBoxBytes, tk,
-                    &bars[B_K_FULL + b], kvh * D + c * 64, w.t * kTile, bz);
-      nk = j + 1;
-      if (j >= 2) ok = mbar_wait(&bars[B_V_EMPTY + b], ((j - 2) >> 1) & 1, p.status, &abort_flag);
-      if (!ok) break;
-      mbar_arrive_expect_tx(&bars[B_V_FULL + b], Lay::kTileBytes);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(smem + Lay::kV + b * Lay::kTileBytes + c * Lay::kBoxBytes, tv,
-                    &bars[B_V_FULL + b], kvh * D + c * 64, w.t * kTile, bz);
-      nv = j + 1;
-    }
-    if (!ok) {
-      // drain: wait (ignoring the abort flag) for the loads already issued
-      // (at most the last two tiles of each ring can still be in flight)
-      mbar_wait(&bars[B_Q_FULL], 0, nullptr, nullptr, 200000000ull);
-      for (int j = (nk > 2 ? nk - 2 : 0); j < nk; ++j)
-        mbar_wait(&bars[B_K_FULL + (j & 1)], (j >> 1) & 1, nullptr, nullptr, 200000000ull);
-      for (int j = (nv > 2 ? nv - 2 : 0); j < nv; ++j)
-        mbar_wait(&bars[B_V_FULL + (j & 1)], (j >> 1) & 1, nullptr, nullptr, 200000000ull);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ===================== MMA issuer
-    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-    bool ok = mbar_wait(&bars[B_Q_FULL], 0, p.status, &abort_flag);
-    const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);  // Q as K-major A
-    auto issue_pv = [&](int i) -> bool {
-      const int c = i & 1;
-      if (!mbar_wait(&bars[B_P_FULL + c], (i >> 1) & 1, p.status, &abort_flag)) return false;
-      if (!mbar_wait(&bars[B_V_FULL + c], (i >> 1) & 1, p.status, &abort_flag)) return false;
-      tc_fence_after_sync();
-      const uint64_t pa = sdesc_sw128(sP + c * Lay::kPBytes, 16, 1024);               // P, K-major A
-      const uint64_t vb = sdesc_sw128(sV + c * Lay::kTileBytes, Lay::kBoxBytes, 1024);  // V, MN-major B
-      const uint32_t acc0 = i > 0 ? 1u : 0u;
-#pragma unroll
-      for (int k = 0; k < kTile / 16; ++k)
-        umma_bf16_ss(tmem + 256, sdesc_step(pa, (k >> 2) * Lay::kBoxBytes + (k & 3) * 32),
-                     sdesc_step(vb, k * 2048), idesc_pv, k > 0 ? 1u : acc0);
-      umma_commit(&bars[B_P_EMPTY + c]);
-      umma_commit(&bars[B_V_EMPTY + c]);
-      return true;
-    };
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int b = j & 1;
-      ok = mbar_wait(&bars[B_K_FULL + b], (j >> 1) & 1, p.status, &abort_flag);
-      if (ok && j >= 2) ok = mbar_wait(&bars[B_S_FREE + b], ((j - 2) >> 1) & 1, p.status, &abort_flag);
-      if (!ok) break;
-      tc_fence_after_sync();
-      const uint64_t k_desc = sdesc_sw128(sK + b * Lay::kTileBytes, 16, 1024);  // K, K-major B
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k >> 2) * Lay::kBoxBytes + (k & 3) * 32;
-        umma_bf16_ss(tmem + b * 128, sdesc_step(q_desc, off), sdesc_step(k_desc, off), idesc_s,
-                     k > 0 ? 1u : 0u);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + Lay::kQ + s * Lay::kTileBytes + c * Lay::kBoxBytes, tq,
+                      &bars[B_Q_FULL + s], h * D + c * 64, tw[1] * kTile, bz);
       }
-      umma_commit(&bars[B_S_FULL + b]);
-      umma_commit(&bars[B_K_EMPTY + b]);
-      if (j >= 1) ok = issue_pv(j - 1);
-    }
-    if (ok) issue_pv(n_tiles - 1);
-    // drain every MMA this thread issued before the CTA may free TMEM
-    umma_commit(&bars[B_DRAIN]);
-    mbar_wait(&bars[B_DRAIN], 0, nullptr, nullptr, 500000000ull);
-  } else if (warp >= 4) {
-    // ===================== softmax warpgroup
-    const int row = threadIdx.x - 128;
-    const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
-    const int64_t qpos = static_cast<int64_t>(q_tile) * kTile + row;
-    const bool row_valid = qpos < p.L;
-    const int qb = row_valid ? static_cast<int>(qpos) / p.M : -1;
-    const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY;
-    float l = 0.f;
-    TileWalk w;
-    w.start(segs, n_segs);
-    bool ok = true;
-    uint8_t* sPbase = smem + Lay::kP;
-    for (int j = 0; j < n_tiles; ++j, w.next()) {
-      const int b = j & 1;
-      if (!mbar_wait_warp(&bars[B_S_FULL + b], (j >> 1) & 1, p.status, &abort_flag)) {
-        ok = false;
-        break;
+      PairWalk w;
+      slot_walk(0, w.w[0]);
+      slot_walk(1, w.w[1]);
+      w.settle();
+      int nk = 0, nv = 0;  // K / V tiles whose loads were issued
+      bool ok = true;
+      for (int m = 0; w.valid() && ok; ++m, w.next()) {
+        const int b = m & 1;
+        const void* tk = w.stream ? static_cast<const void*>(&tm_k1) : static_cast<const void*>(&tm_k0);
+        const void* tv = w.stream ? static_cast<const void*>(&tm_v1) : static_cast<const void*>(&tm_v0);
+        if (m >= 2) ok = mbar_wait(&bars[B_K_EMPTY + b], ((m - 2) >> 1) & 1, p.status, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars[B_K_FULL + b], Lay::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + Lay::kK + b * Lay::kTileBytes + c * Lay::kBoxBytes, tk,
+                      &bars[B_K_FULL + b], kvh * D + c * 64, w.t * kTile, bz);
+        nk = m + 1;
+        if (m >= 2) ok = mbar_wait(&bars[B_V_EMPTY + b], ((m - 2) >> 1) & 1, p.status, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars[B_V_FULL + b], Lay::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + Lay::kV + b * Lay::kTileBytes + c * Lay::kBoxBytes, tv,
+                      &bars[B_V_FULL + b], kvh * D + c * 64, w.t * kTile, bz);
+        nv = m + 1;
       }
-      tc_fence_after_sync();
-      float s[kTile];
+      if (!ok) {
+        // drain: wait (ignoring the abort flag) for the loads already issued
+        for (int s = 0; s < n_slots; ++s)
+          mbar_wait(&bars[B_Q_FULL + s], 0, nullptr, nullptr, 200000000ull);
+        for (int m = (nk > 2 ? nk - 2 : 0); m < nk; ++m)
+          mbar_wait(&bars[B_K_FULL + (m & 1)], (m >> 1) & 1, nullptr, nullptr, 200000000ull);
+        for (int m = (nv > 2 ? nv - 2 : 0); m < nv; ++m)
+          mbar_wait(&bars[B_V_FULL + (m & 1)], (m >> 1) & 1, nullptr, nullptr, 200000000ull);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ===================== MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+      bool ok = true;
+      for (int s = 0; s < n_slots && ok; ++s) ok = mbar_wait(&bars[B_Q_FULL + s], 0, p.status, abort_flag);
+      int npv[2] = {0, 0};  // PV issued per slot
+      // S_s = Q_s K^T of ring stage b into slot s's S columns
+      auto issue_s = [&](int s, int b) -> bool {
+        if (npv[s] > 0 && !mbar_wait(&bars[B_PV_DONE + s], (npv[s] - 1) & 1, p.status, abort_flag))
+          return false;  // its last PV still reads the P held there
+        tc_fence_after_sync();
+        const uint64_t q_desc = sdesc_sw128(smem_u32(smem + Lay::kQ + s * Lay::kTileBytes), 16, 1024);
+        const uint64_t k_desc = sdesc_sw128(smem_u32(smem + Lay::kK + b * Lay::kTileBytes), 16, 1024);
 #pragma unroll
-      for (int c = 0; c < kTile / 32; ++c) tmem_ld32(tmem + lane_base + b * 128 + c * 32, s + c * 32);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_S_FREE + b]);
-
-      const bool ragged = (static_cast<int64_t>(w.t) + 1) * kTile > p.L;
-      float mx = -INFINITY;
-      if ((w.flags & 1) || ragged || !row_valid) {
-        // the allowed keys of this query row form one range [lo, hi)
-        int lo, hi;
-        allowed_key_range(q_stream, w.stream, qb, p.M, p.L, row_valid, lo, hi);
-        lo -= w.t * kTile;
-        hi -= w.t * kTile;
-#pragma unroll
-        for (int c = 0; c < kTile; ++c) {
-          s[c] = (c >= lo && c < hi) ? s[c] * sl2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * Lay::kBoxBytes + (k & 3) * 32;
+          umma_bf16_ss(tmem + s * 128, sdesc_step(q_desc, off), sdesc_step(k_desc, off), idesc_s,
+                       k > 0 ? 1u : 0u);
         }
-      } else {
+        umma_commit(&bars[B_S_FULL + s]);
+        return true;
+      };
+      // O_s += P_s V of ring stage b, P_s (bf16 pairs) in slot s's S columns
+      auto issue_pv = [&](int s, int b) -> bool {
+        if (!mbar_wait(&bars[B_P_FULL + s], npv[s] & 1, p.status, abort_flag)) return false;
+        tc_fence_after_sync();
+        const uint64_t vb = sdesc_sw128(smem_u32(smem + Lay::kV + b * Lay::kTileBytes), Lay::kBoxBytes,
+                                        1024);  // V, MN-major B
+        const uint32_t acc0 = npv[s] > 0 ? 1u : 0u;
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) {
-          s[c] *= sl2;
-          mx = fmaxf(mx, s[c]);
+        for (int k = 0; k < kTile / 16; ++k)
+          umma_bf16_ts(tmem + Lay::kColO + s * D, tmem + s * 128 + k * 8, sdesc_step(vb, k * 2048),
+                       idesc_pv, k > 0 ? 1u : acc0);
+        umma_commit(&bars[B_PV_DONE + s]);
+        ++npv[s];
+        return true;
+      };
+      PairWalk w;
+      slot_walk(0, w.w[0]);
+      slot_walk(1, w.w[1]);
+      w.settle();
+      int prev_in[2] = {0, 0};
+      int m = 0;
+      for (; w.valid() && ok; ++m, w.next()) {
+        const int b = m & 1;
+        const int pb = (m - 1) & 1;
+        if (m > 0) ok = mbar_wait(&bars[B_V_FULL + pb], ((m - 1) >> 1) & 1, p.status, abort_flag);
+        if (ok) ok = mbar_wait(&bars[B_K_FULL + b], (m >> 1) & 1, p.status, abort_flag);
+        // slot by slot: the PV of the previous tile, then the S of this one,
+        // so that one slot's softmax runs while the other slot's MMAs do
+        const int in[2] = {w.in0, w.in1};
+        for (int s = 0; s < 2 && ok; ++s) {
+          if (prev_in[s]) ok = issue_pv(s, pb);
+          if (ok && in[s]) ok = issue_s(s, b);
         }
+        if (!ok) break;
+        if (m > 0) umma_commit(&bars[B_V_EMPTY + pb]);
+        umma_commit(&bars[B_K_EMPTY + b]);
+        prev_in[0] = w.in0;
+        prev_in[1] = w.in1;
       }
-      const float m_new = fmaxf(m_ref, mx);
-      const bool need = m_new > m_ref + kRescaleThreshold;  // false while both are -inf
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds PV_0..PV_{j-1} scaled by the old reference: wait for PV_{j-1}
-        if (!mbar_wait_warp(&bars[B_P_EMPTY + ((j - 1) & 1)], ((j - 1) >> 1) & 1, p.status, &abort_flag)) {
+      if (ok && m > 0) {
+        const int pb = (m - 1) & 1;
+        ok = mbar_wait(&bars[B_V_FULL + pb], ((m - 1) >> 1) & 1, p.status, abort_flag);
+        for (int s = 0; s < 2 && ok; ++s)
+          if (prev_in[s]) ok = issue_pv(s, pb);
+      }
+      // drain every MMA this thread issued before the CTA may free TMEM
+      umma_commit(&bars[B_DRAIN]);
+      mbar_wait(&bars[B_DRAIN], 0, nullptr, nullptr, 500000000ull);
+    }
+  } else {
+    setmaxnreg_inc<kRegsSoftmax>();
+    // ===================== softmax warpgroup of slot s
+    const int s = (warp - 4) >> 2;
+    const int row = threadIdx.x - 128 * (1 + s);
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t colS = s * 128;
+    const uint32_t colO = Lay::kColO + s * D;
+    const int n_tiles = slot_tiles(s);
+    if (n_tiles > 0) {
+      const int32_t* tw = task_words(s);
+      const int q_stream = tw[0];
+      const int q_tile = tw[1];
+      const int part = tw[2];
+      const int64_t qpos = static_cast<int64_t>(q_tile) * kTile + row;
+      const bool row_valid = qpos < p.L;
+      const int qb = row_valid ? static_cast<int>(qpos) / p.M : -1;
+      const float sl2 = p.scale_log2;
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      SlotWalk w;
+      slot_walk(s, w);
+      bool ok = true;
+      for (int j = 0; j < n_tiles; ++j, w.next()) {
+        if (!mbar_wait_warp(&bars[B_S_FULL + s], j & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const float alpha = need ? exp2f(m_ref - m_new) : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tmem_ld32(tmem + lane_base + 256 + c * 32, o);
+        float sv[kTile];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(tmem + lane_base + 256 + c * 32, o);
-        }
-      }
-      if (need) {
-        l *= exp2f(m_ref - m_new);  // 0 when m_ref was -inf
-        m_ref = m_new;
-      }
-      const float mref_safe = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float rs = 0.f;
+        for (int c = 0; c < kTile / 32; c += 2)
+          tmem_ld32x2(tmem + lane_base + colS + c * 32, tmem + lane_base + colS + (c + 1) * 32,
+                      sv + c * 32, sv + (c + 1) * 32);
+        const bool ragged = (static_cast<int64_t>(w.t) + 1) * kTile > p.L;
+        float mx = -INFINITY;
+        if ((w.flags & 1) || ragged || !row_valid) {
+          // the allowed keys of this query row form one range [lo, hi)
+          int lo, hi;
+          allowed_key_range(q_stream, w.stream, qb, p.M, p.L, row_valid, lo, hi);
+          lo -= w.t * kTile;
+          hi -= w.t * kTile;
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) {
-        s[c] = ex2_approx(s[c] - mref_safe);
-        rs += s[c];
-      }
-      l += rs;
-      if (j >= 2 && !mbar_wait_warp(&bars[B_P_EMPTY + b], ((j - 2) >> 1) & 1, p.status, &abort_flag)) {
-        ok = false;
-        break;
-      }
-      uint8_t* pb = sPbase + b * Lay::kPBytes;
+          for (int c = 0; c < kTile; ++c) {
+            sv[c] = (c >= lo && c < hi) ? sv[c] * sl2 : -INFINITY;
+            mx = fmaxf(mx, sv[c]);
+          }
+        } else {
 #pragma unroll
-      for (int ch = 0; ch < kTile / 8; ++ch) {
-        uint4 v;
-        v.x = pack_bf16x2(s[ch * 8 + 0], s[ch * 8 + 1]);
-        v.y = pack_bf16x2(s[ch * 8 + 2], s[ch * 8 + 3]);
-        v.z = pack_bf16x2(s[ch * 8 + 4], s[ch * 8 + 5]);
-        v.w = pack_bf16x2(s[ch * 8 + 6], s[ch * 8 + 7]);
-        *reinterpret_cast<uint4*>(pb + (ch >> 3) * Lay::kBoxBytes + sw128_offset(row, ch & 7)) = v;
-      }
-      fence_proxy_async_smem();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_P_FULL + b]);
-    }
-    // ---- epilogue: wait for the last PV, normalise, store
-    if (ok && mbar_wait_warp(&bars[B_P_EMPTY + ((n_tiles - 1) & 1)], ((n_tiles - 1) >> 1) & 1, p.status,
-                        &abort_flag)) {
-      tc_fence_after_sync();
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const float lse = (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
-      if (p.partial_mode) {
-        const int64_t prow = ((static_cast<int64_t>(part) * 2 + q_stream) * p.batch + bz);
-        float* dst = p.part_o + (prow * p.L + qpos) * p.Hq * D + static_cast<int64_t>(h) * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tmem_ld32(tmem + lane_base + 256 + c * 32, o);
-          if (row_valid) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(dst + c * 32 + i) =
-                  make_float4(o[i] * inv_l, o[i + 1] * inv_l, o[i + 2] * inv_l, o[i + 3] * inv_l);
+          for (int c = 0; c < kTile; ++c) {
+            sv[c] *= sl2;
+            mx = fmaxf(mx, sv[c]);
           }
         }
-        if (row_valid) p.part_lse[(prow * p.Hq + h) * p.L + qpos] = lse;
-      } else {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(q_stream ? p.o[1] : p.o[0]) +
-                             ((static_cast<int64_t>(bz) * p.L + qpos) * p.Hq + h) * D;
+        const float m_new = fmaxf(m_ref, mx);
+        const bool need = m_new > m_ref + kRescaleThreshold;  // false while both are -inf
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // O holds PV_0..PV_{j-1} scaled by the old reference; PV_{j-1} is
+          // complete: the S this tile read was issued after it
+          const float alpha = need ? exp2f(m_ref - m_new) : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tmem_ld32(tmem + lane_base + 256 + c * 32, o);
-          if (row_valid) {
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tmem + lane_base + colO + c * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 v;
-              v.x = pack_bf16x2(o[i] * inv_l, o[i + 1] * inv_l);
-              v.y = pack_bf16x2(o[i + 2] * inv_l, o[i + 3] * inv_l);
-              v.z = pack_bf16x2(o[i + 4] * inv_l, o[i + 5] * inv_l);
-              v.w = pack_bf16x2(o[i + 6] * inv_l, o[i + 7] * inv_l);
-              *reinterpret_cast<uint4*>(dst + c * 32 + i) = v;
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tmem + lane_base + colO + c * 32, o);
+          }
+        }
+        if (need) {
+          l *= exp2f(m_ref - m_new);  // 0 when m_ref was -inf
+          m_ref = m_new;
+        }
+        const float mref_safe = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float rs = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float packed[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float e0 = ex2_approx(sv[half * 64 + 2 * c] - mref_safe);
+            const float e1 = ex2_approx(sv[half * 64 + 2 * c + 1] - mref_safe);
+            rs += e0 + e1;
+            packed[c] = __uint_as_float(pack_bf16x2(e0, e1));
+          }
+          tmem_st32(tmem + lane_base + colS + half * 32, packed);
+        }
+        l += rs;
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_P_FULL + s]);
+      }
+      // ---- epilogue: wait for the last PV, normalise, store
+      if (ok && mbar_wait_warp(&bars[B_PV_DONE + s], (n_tiles - 1) & 1, p.status, abort_flag)) {
+        tc_fence_after_sync();
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const float lse = (l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (p.partial_mode) {
+          const int64_t prow = ((static_cast<int64_t>(part) * 2 + q_stream) * p.batch + bz);
+          float* dst = p.part_o + (prow * p.L + qpos) * p.Hq * D + static_cast<int64_t>(h) * D;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tmem + lane_base + colO + c * 32, o);
+            if (row_valid) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(dst + c * 32 + i) =
+                    make_float4(o[i] * inv_l, o[i + 1] * inv_l, o[i + 2] * inv_l, o[i + 3] * inv_l);
             }
           }
+          if (row_valid) p.part_lse[(prow * p.Hq + h) * p.L + qpos] = lse;
+        } else {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(q_stream ? p.o[1] : p.o[0]) +
+                               ((static_cast<int64_t>(bz) * p.L + qpos) * p.Hq + h) * D;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tmem + lane_base + colO + c * 32, o);
+            if (row_valid) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 8) {
+                uint4 v;
+                v.x = pack_bf16x2(o[i] * inv_l, o[i + 1] * inv_l);
+                v.y = pack_bf16x2(o[i + 2] * inv_l, o[i + 3] * inv_l);
+                v.z = pack_bf16x2(o[i + 4] * inv_l, o[i + 5] * inv_l);
+                v.w = pack_bf16x2(o[i + 6] * inv_l, o[i + 7] * inv_l);
+                *reinterpret_cast<uint4*>(dst + c * 32 + i) = v;
+              }
+            }
+          }
+          if (row_valid)
+            p.lse[((static_cast<int64_t>(bz) * 2 + q_stream) * p.Hq + h) * p.L + qpos] = lse;
         }
-        if (row_valid)
-          p.lse[((static_cast<int64_t>(bz) * 2 + q_stream) * p.Hq + h) * p.L + qpos] = lse;
       }
     }
   }
@@ -410,16 +476,24 @@ static cudaError_t launch_fwd_d(const CUtensorMap* maps, const FwdParams& p, int
                                 cudaStream_t stream) {
   using Lay = FwdLayout<D>;
   static bool configured = false;
+  static int launch_regs = 0;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay::kDynSmem);
     if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fwd_kernel<D>);
+    if (e != cudaSuccess) return e;
+    launch_regs = fa.numRegs;
     configured = true;
   }
-  const int64_t grid = static_cast<int64_t>(n_tasks) * p.Hq * p.batch;
+  // setmaxnreg.inc would wait forever if the budgets exceeded the launch
+  // allocation: refuse to launch instead
+  if (launch_regs * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+  const int64_t grid = static_cast<int64_t>((n_tasks + 1) / 2) * p.Hq * p.batch;
   if (grid <= 0) return cudaSuccess;
   fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, Lay::kDynSmem, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p, n_tasks);
   return cudaGetLastError();
 }
 

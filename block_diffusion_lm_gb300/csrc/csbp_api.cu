@@ -16,8 +16,6 @@ namespace csbp {
 
 cudaError_t launch_fwd(int d, const CUtensorMap* maps, const FwdParams& p, int n_tasks,
                        cudaStream_t stream);
-cudaError_t launch_fwd_pair(int d, const CUtensorMap* maps, const FwdParams& p, int n_tasks,
-                       cudaStream_t stream);
 cudaError_t launch_bwd(int d, const CUtensorMap* maps, const BwdParams& p, int n_tasks,
                        cudaStream_t stream);
 int bwd_query_box_rows();
@@ -316,11 +314,7 @@ extern "C" csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inp
     if (launch_fill(fp.part_lse, n_lse, -INFINITY, stream) != cudaSuccess) return CSBP_ERR_CUDA;
   }
   const int timed = timer_begin(0, stream);
-  // fused problems pair query tiles per CTA (two softmax warpgroups); the
-  // per-part tasks of a sharded problem run one per CTA
-  const cudaError_t fe = fp.partial_mode
-                             ? launch_fwd(p.d, maps, fp, info->n_fwd_tasks, stream)
-                             : launch_fwd_pair(p.d, maps, fp, info->n_fwd_tasks, stream);
+  const cudaError_t fe = launch_fwd(p.d, maps, fp, info->n_fwd_tasks, stream);
   timer_end(timed, stream);
   if (fe != cudaSuccess) return CSBP_ERR_CUDA;
   if (p.P > 1) {

@@ -163,7 +163,9 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
               t.cost += segs[i].end - segs[i].begin;
             }
           if (t.segs.empty()) continue;
-          t.canon = ((int64_t)qs * nT + qt) * (P + 1) + part;
+          // equal-cost tasks of one part and copy sit next to each other, so
+          // the two query tiles a forward CTA pairs share their key tiles
+          t.canon = ((int64_t)part * 2 + qs) * nT + qt;
           fwd.push_back(std::move(t));
         }
       }
