@@ -86,6 +86,25 @@ def recorded_traffic(workload):
         return None
 
 
+# --------------------------------------------------------------- ranks
+def max_over_ranks(value, device):
+    """The largest of every rank's value (the slowest rank sets the job's
+    time); the value itself when not running under torch.distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    x = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(x, op=dist.ReduceOp.MAX)
+    return x.item()
+
+
+def whole_job_tflops(world, flops_per_rank_step, ms_per_step):
+    """Useful TFLOP/s of the whole job: every rank does one replica's step in
+    ms_per_step (the max over ranks)."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -306,13 +325,11 @@ def main():
     total_ms = start_all.elapsed_time(end_all)
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
     bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    total_ms = max_over_ranks(total_ms, dev)
     if world > 1:
-        x = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        total_ms = x.item()
         dist.barrier()
     ms_per_step = total_ms / args.steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, ms_per_step)
 
     # ---------------- end to end through the public API with host buffers
     e2e = None
@@ -418,12 +435,8 @@ def run_e2e(args, w, t, attn, out, grads, stream, dev, world, flops, in_bytes):
     e1 = torch.cuda.Event(enable_timing=True)
     run(e2e_steps, e0, e1)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        x = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        e2e_ms = x.item()
-    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    e2e_value = whole_job_tflops(world, flops, e2e_ms)
     return {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": in_bytes,
             "d2h_bytes_per_step": out_bytes, "overlap": "copies on separate streams, 2 buffer sets"}
 

@@ -1,0 +1,50 @@
+"""Multi-rank logic of bench.py on CPU: two gloo ranks (127.0.0.1), each with
+its own step time; every rank must see the slowest one, and the whole-job
+value must count both replicas."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, ms, q):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.max_over_ranks(ms[rank], "cpu")
+        q.put((rank, got, bench.whole_job_tflops(world, 2e12, got)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    world, port = 2, _free_port()
+    ms = [18.5, 21.25]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank, args=(r, world, port, ms, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(world))
+    for rank, got, tflops in res:
+        assert got == pytest.approx(21.25)
+        assert tflops == pytest.approx(2 * 2e12 / 21.25e-3 / 1e12)
+
+
+def test_single_process_values_pass_through():
+    assert bench.max_over_ranks(3.5, "cpu") == 3.5
+    assert bench.whole_job_tflops(1, 1e12, 1000.0) == pytest.approx(1.0)
