@@ -207,11 +207,10 @@ def cpu_oracle_sample(w, seconds, seed=7):
         h = int(rng.integers(0, w.Hq))
         samples = [(int(rng.choice(streams)), int(rng.integers(0, L)), h) for _ in range(batch_rows)]
         O.sampled_rows(fv["q_clean"], fv["k_clean"], fv["v_clean"], fv["q_corr"], fv["k_corr"],
-                       fv["v_corr"], fv["do_clean"], fv["do_corr"], w.M, w.scale, samples)
+                       fv["v_corr"], fv["do_clean"], fv["do_corr"], w.M, w.scale, samples,
+                       w.window, w.clean_causal)
         for qs, i, _ in samples:
-            b = i // w.M
-            n_allowed = (b + 1) * w.M  # both copies: M(b+1) visible keys
-            useful += 4.0 * w.d * n_allowed * 3.5
+            useful += 4.0 * w.d * w.keys_of_row(qs, i) * 3.5
         rows_done += batch_rows
     dt = time.perf_counter() - t0
     del G
@@ -287,7 +286,8 @@ def main():
 
     t = make_inputs(w, dev)
     attn = csbp.BlockDiffusionAttention(w.batch, w.L, w.M, w.Hq, w.Hkv, w.d, P=w.P,
-                                        has_clean_queries=w.has_clean_queries, device=dev)
+                                        has_clean_queries=w.has_clean_queries, device=dev,
+                                        window=w.window, clean_causal=w.clean_causal)
     out = attn.alloc_outputs()
     grads = attn.alloc_grads()
     in_bytes = sum(v.numel() * v.element_size() for v in t.values() if v is not None)

@@ -144,23 +144,26 @@ struct QWalk {
   }
 };
 
-// Query positions [lo, hi) that may read key block kb of copy k_stream, for
-// queries of copy q_stream: clean keys are read by clean queries of the same
-// or later blocks and by corrupted queries of later blocks; corrupted keys
-// only by corrupted queries of their own block.
-__device__ __forceinline__ void allowed_query_range(int q_stream, int k_stream, int kb, int M,
-                                                    int L, bool k_valid, int& lo, int& hi) {
+// Query positions [lo, hi) of copy q_stream that may read key position kpos
+// (block kb) of copy k_stream: clean keys are read by clean queries of the
+// same or later blocks (queries >= kpos when token-causal) and by corrupted
+// queries of later blocks; corrupted keys only by corrupted queries of their
+// own block; a window W > 0 also drops queries W or more positions after.
+__device__ __forceinline__ void allowed_query_range(int q_stream, int k_stream, int kpos, int kb,
+                                                    int M, int L, int window, int clean_causal,
+                                                    bool k_valid, int& lo, int& hi) {
   if (!k_valid || (q_stream == 0 && k_stream == 1)) {
     lo = hi = 0;
     return;
   }
   if (k_stream == 0) {
-    lo = (q_stream == 0) ? kb * M : (kb + 1) * M;
+    lo = (q_stream == 0) ? (clean_causal ? kpos : kb * M) : (kb + 1) * M;
     hi = L;
   } else {
     lo = kb * M;
     hi = min((kb + 1) * M, L);
   }
+  if (window > 0) hi = min(hi, kpos + window);
 }
 
 // S^T (or dP^T) of one step: M = 128 key rows, N = 128 query rows, K = d.
@@ -424,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (masked) {
         // allowed query positions of this key row form one range [lo, hi)
         int lo, hi;
-        allowed_query_range(qs, k_stream, kb, p.M, p.L, k_valid, lo, hi);
+        allowed_query_range(qs, k_stream, kpos, kb, p.M, p.L, p.window, p.clean_causal, k_valid,
+                            lo, hi);
         lo -= q0;
         hi -= q0;
 #pragma unroll

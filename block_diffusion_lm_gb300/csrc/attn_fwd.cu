@@ -123,11 +123,13 @@ struct PairWalk {
   }
 };
 
-// Key positions [lo, hi) of copy k_stream that a query of block qb of copy
-// q_stream may read: clean queries read clean keys of blocks <= qb;
-// corrupted queries read clean keys of blocks < qb and the corrupted keys of
-// their own block.
-__device__ __forceinline__ void allowed_key_range(int q_stream, int k_stream, int qb, int M, int L,
+// Key positions [lo, hi) of copy k_stream that query position qpos (block qb)
+// of copy q_stream may read: clean queries read clean keys of blocks <= qb
+// (keys <= qpos when token-causal); corrupted queries read clean keys of
+// blocks < qb and the corrupted keys of their own block; a window W > 0 also
+// drops keys W or more positions back.
+__device__ __forceinline__ void allowed_key_range(int q_stream, int k_stream, int qpos, int qb,
+                                                  int M, int L, int window, int clean_causal,
                                                   bool row_valid, int& lo, int& hi) {
   lo = 0;
   if (!row_valid || (q_stream == 0 && k_stream == 1)) {
@@ -135,7 +137,7 @@ __device__ __forceinline__ void allowed_key_range(int q_stream, int k_stream, in
     return;
   }
   if (q_stream == 0) {
-    hi = (qb + 1) * M;
+    hi = clean_causal ? qpos + 1 : (qb + 1) * M;
   } else if (k_stream == 0) {
     hi = qb * M;
   } else {
@@ -143,6 +145,7 @@ __device__ __forceinline__ void allowed_key_range(int q_stream, int k_stream, in
     hi = (qb + 1) * M;
   }
   hi = min(hi, L);
+  if (window > 0) lo = max(lo, qpos - window + 1);
 }
 
 template <int D>
@@ -364,7 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((w.flags & 1) || ragged || !row_valid) {
           // the allowed keys of this query row form one range [lo, hi)
           int lo, hi;
-          allowed_key_range(q_stream, w.stream, qb, p.M, p.L, row_valid, lo, hi);
+          allowed_key_range(q_stream, w.stream, static_cast<int>(qpos), qb, p.M, p.L, p.window,
+                            p.clean_causal, row_valid, lo, hi);
           lo -= w.t * kTile;
           hi -= w.t * kTile;
 #pragma unroll

@@ -299,6 +299,8 @@ extern "C" csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inp
   fp.Hkv = p.Hkv;
   fp.G = p.Hq / p.Hkv;
   fp.batch = p.batch;
+  fp.window = p.window;
+  fp.clean_causal = p.clean_causal;
   fp.scale_log2 = p.scale * 1.4426950408889634f;
   fp.o[0] = o_clean;
   fp.o[1] = o_corr;
@@ -407,6 +409,8 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
   bp.Hkv = p.Hkv;
   bp.G = p.Hq / p.Hkv;
   bp.batch = p.batch;
+  bp.window = p.window;
+  bp.clean_causal = p.clean_causal;
   bp.scale_log2 = p.scale * 1.4426950408889634f;
   bp.scale = p.scale;
   bp.lse = lse;

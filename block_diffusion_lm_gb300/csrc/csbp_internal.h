@@ -31,6 +31,7 @@ struct FwdParams {
   const int32_t* tasks;  // device: fwd task records
   const int32_t* segs;   // device: fwd segment records
   int32_t L, M, Hq, Hkv, G, batch;
+  int32_t window, clean_causal;  // mask options (0 = none / block-causal)
   float scale_log2;      // softmax scale * log2(e)
   void* o[2];            // bf16 outputs per query stream
   float* lse;            // [batch][2][Hq][L]
@@ -50,6 +51,7 @@ struct BwdParams {
   const int32_t* tasks;  // device: bwd task records
   const int32_t* segs;   // device: bwd segment records
   int32_t L, M, Hq, Hkv, G, batch;
+  int32_t window, clean_causal;  // mask options (0 = none / block-causal)
   float scale_log2;
   float scale;
   const float* lse;      // [batch][2][Hq][L]

@@ -22,6 +22,49 @@
 
 namespace csbp {
 
+// Allowed key positions [lo, hi) of copy k_stream for query position i of
+// copy q_stream, with the optional window (keys less than `window` positions
+// back) and token-causal clean attention; both bounds are non-decreasing in i.
+void key_range(int q_stream, int k_stream, int64_t i, int64_t L, int64_t M, int64_t window,
+               bool clean_causal, int64_t& lo, int64_t& hi) {
+  const int64_t b = i / M;
+  lo = 0;
+  if (q_stream == 0 && k_stream == 1) {
+    hi = 0;
+    return;
+  }
+  if (q_stream == 0) {
+    hi = clean_causal ? i + 1 : std::min((b + 1) * M, L);
+  } else if (k_stream == 0) {
+    hi = b * M;
+  } else {
+    lo = b * M;
+    hi = std::min((b + 1) * M, L);
+  }
+  if (window > 0) lo = std::max(lo, i - window + 1);
+}
+
+// 0 = no allowed entry, 1 = some (partial), 2 = all entries allowed; from the
+// rows' key ranges (non-decreasing, so the first and last rows bound the
+// hull and the tightest row; only tiles between the two are scanned)
+int classify_tile_ranges(int q_stream, int64_t qt, int k_stream, int64_t kt, int64_t L,
+                         int64_t M, int64_t T, int64_t window, bool clean_causal) {
+  const int64_t r0 = qt * T, r1 = std::min(r0 + T, L) - 1;
+  const int64_t c0 = kt * T, c1 = std::min(c0 + T, L) - 1;
+  if (r0 > r1 || c0 > c1) return 0;
+  int64_t lo0, hi0, lo1, hi1;
+  key_range(q_stream, k_stream, r0, L, M, window, clean_causal, lo0, hi0);
+  key_range(q_stream, k_stream, r1, L, M, window, clean_causal, lo1, hi1);
+  if (lo0 > c1 || hi1 <= c0) return 0;      // outside every row's range
+  if (lo1 <= c0 && hi0 > c1) return 2;      // inside every row's range
+  for (int64_t i = r0; i <= r1; ++i) {
+    int64_t lo, hi;
+    key_range(q_stream, k_stream, i, L, M, window, clean_causal, lo, hi);
+    if (lo <= c1 && hi > c0 && lo < hi) return 1;
+  }
+  return 0;
+}
+
 // 0 = no allowed entry, 1 = some (partial), 2 = all entries allowed.
 int classify_tile(int q_stream, int64_t qt, int k_stream, int64_t kt, int64_t L, int64_t M,
                   int64_t T) {
@@ -82,6 +125,7 @@ csbp_status validate_problem(const csbp_problem* p) {
   if (!(p->scale > 0.0f) || p->scale != p->scale) return CSBP_ERR_INVALID;
   if (p->tile_q < 1 || p->tile_kv < 1) return CSBP_ERR_INVALID;
   if (p->has_clean_queries != 0 && p->has_clean_queries != 1) return CSBP_ERR_INVALID;
+  if (p->window < 0 || (p->clean_causal != 0 && p->clean_causal != 1)) return CSBP_ERR_INVALID;
   if (p->d != 64 && p->d != 128) return CSBP_ERR_UNSUPPORTED;
   if (p->tile_q != p->tile_kv) return CSBP_ERR_UNSUPPORTED;
   if (p->P > 1) {
@@ -108,6 +152,12 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
   const int64_t B = L / M;
   const int64_t nT = (L + T - 1) / T;
   if (nT > (int64_t)1 << 30) return CSBP_ERR_UNSUPPORTED;
+  const int64_t W = problem->window;
+  const bool causal = problem->clean_causal != 0;
+  auto classify = [&](int qs, int64_t qt, int ks, int64_t kt) {
+    return (W > 0 || causal) ? classify_tile_ranges(qs, qt, ks, kt, L, M, T, W, causal)
+                             : classify_tile(qs, qt, ks, kt, L, M, T);
+  };
 
   // ---- ownership (P == 1: one shard owning both chunks)
   std::vector<int32_t> co(2 * P);
@@ -142,7 +192,7 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
       std::vector<int32_t> seg_part;
       for (int ks = 0; ks < 2; ++ks) {
         for (int64_t kt = 0; kt < nT; ++kt) {
-          const int cls = classify_tile(qs, qt, ks, kt, L, M, T);
+          const int cls = classify(qs, qt, ks, kt);
           if (!cls) continue;
           ++pairs;
           const int32_t part = (ks == 1) ? P : clean_part(kt * T);
@@ -182,7 +232,7 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
       for (int qs = q_stream0; qs < 2; ++qs) {
         // only a band of query tiles can read key tile kt; scan all for clarity
         for (int64_t qt = 0; qt < nT; ++qt) {
-          const int cls = classify_tile(qs, qt, ks, kt, L, M, T);
+          const int cls = classify(qs, qt, ks, kt);
           if (!cls) continue;
           push_tile(t.segs, dummy_part, qs, (int32_t)qt, cls, 0);
           t.cost += 1;

@@ -32,6 +32,8 @@ class Workload:
     has_clean_queries: bool = True
     k_scale_range: tuple | None = None   # per-KV-head K scale ~ U(lo, hi)
     seed: int = 1234
+    window: int = 0                      # keys less than `window` positions back (0: all)
+    clean_causal: bool = False           # clean queries token-causal (else block-causal)
 
     @property
     def scale(self) -> float:
@@ -43,9 +45,30 @@ class Workload:
 
     def pairs_per_head(self) -> int:
         """Allowed (query, key) pairs per query head: L(L+M) with clean
-        queries, L(L+M)/2 with corrupted queries only."""
-        full = self.L * (self.L + self.M)
-        return full if self.has_clean_queries else full // 2
+        queries, L(L+M)/2 with corrupted queries only; with a window or
+        token-causal clean queries, the sum of each row's key-range length."""
+        if self.window <= 0 and not self.clean_causal:
+            full = self.L * (self.L + self.M)
+            return full if self.has_clean_queries else full // 2
+        i = torch.arange(self.L, dtype=torch.int64)
+        b = i // self.M
+        lo = (i - self.window + 1).clamp(min=0) if self.window > 0 else torch.zeros_like(i)
+        n = (b * self.M - lo).clamp(min=0)                                  # corrupted q, clean k
+        n += ((b + 1) * self.M - torch.maximum(b * self.M, lo)).clamp(min=0)  # corrupted q, own block
+        if self.has_clean_queries:
+            hi = (i + 1) if self.clean_causal else (b + 1) * self.M
+            n += (hi - lo).clamp(min=0)                                       # clean q, clean k
+        return int(n.sum())
+
+    def keys_of_row(self, q_stream: int, i: int) -> int:
+        """Allowed keys of query row i of one copy (0 clean, 1 corrupted),
+        counted the way pairs_per_head counts them."""
+        b = i // self.M
+        lo = max(0, i - self.window + 1) if self.window > 0 else 0
+        if q_stream == 1:
+            return max(0, b * self.M - lo) + max(0, (b + 1) * self.M - max(b * self.M, lo))
+        hi = i + 1 if self.clean_causal else (b + 1) * self.M
+        return max(0, hi - lo)
 
     def useful_fwd_flops(self) -> float:
         """QK^T and PV over allowed pairs: 4 d flops per pair per query head."""
@@ -69,6 +92,8 @@ WORKLOADS = {
     # drafter: corrupted queries only over a 1M clean context
     "drafter": Workload("drafter", 1, 1048576, 16, 32, 8, 128,
                         has_clean_queries=False, seed=1238),
+    # sliding-window layer: the dense shapes with a 1,024-token window
+    "window1k": Workload("window1k", 1, 16384, 32, 40, 8, 128, window=1024, seed=1239),
 }
 
 

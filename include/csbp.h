@@ -78,6 +78,12 @@ typedef struct {
   int32_t tile_q, tile_kv;
   int32_t has_clean_queries;
   float scale;
+  int32_t window;       /* 0: none; W > 0: a query reads only keys less than W
+                           positions back (i - j < W, positions within each
+                           copy), on top of the block rules (sliding-window
+                           layers, [Blog] "实验数字：256K 上下文下的主结果")      */
+  int32_t clean_causal; /* 0: clean queries block-causal over the clean copy;
+                           1: token-causal (key j <= query i)             */
 } csbp_problem;
 
 /* Device input tensors, bf16 [batch][L][H][d] contiguous (H = Hq for q,

@@ -54,53 +54,77 @@ CORR = 1
 # Mask  ([Blog] "传统上下文并行为什么会传错东西" and "CSBP：BP 管损坏块，CP 管干净上下文";
 #        [Project] "Method")
 # --------------------------------------------------------------------------
-def allowed(q_stream: int, i: int, k_stream: int, j: int, M: int) -> bool:
+def allowed(q_stream: int, i: int, k_stream: int, j: int, M: int, window: int = 0,
+            clean_causal: bool = False) -> bool:
     """Scalar mask predicate: may query (q_stream, i) read key (k_stream, j)?
 
     corrupted q -> corrupted k : same block (bidirectional inside the block)
     corrupted q -> clean k     : strictly earlier block  (K^clean_<b)
-    clean q     -> clean k     : same or earlier block   (block-causal reading)
+    clean q     -> clean k     : same or earlier block   (block-causal reading);
+                                 with clean_causal, j <= i (token-causal)
     clean q     -> corrupted k : never (corrupted K/V are read by their own
                                  block only)
+
+    window > 0 keeps, of those keys, the ones less than `window` positions
+    before the query (i - j < window, positions within each copy): the
+    sliding-window attention layers of [Blog] "实验数字：256K 上下文下的主结果"
+    (25 of DiffusionGemma's 30 layers use a 1,024-token window) and [Project]
+    "Where does the time go? Attention traffic at 256K"; reading: the window
+    bounds only how far back a key may lie, the block rules above still apply.
     """
     bi, bj = i // M, j // M
     if q_stream == CORR and k_stream == CORR:
-        return bj == bi
-    if q_stream == CORR and k_stream == CLEAN:
-        return bj < bi
-    if q_stream == CLEAN and k_stream == CLEAN:
-        return bj <= bi
-    return False
+        ok = bj == bi
+    elif q_stream == CORR and k_stream == CLEAN:
+        ok = bj < bi
+    elif q_stream == CLEAN and k_stream == CLEAN:
+        ok = (j <= i) if clean_causal else (bj <= bi)
+    else:
+        ok = False
+    return ok and (window <= 0 or i - j < window)
 
 
-def bd_mask(L: int, M: int) -> np.ndarray:
+def bd_mask(L: int, M: int, window: int = 0, clean_causal: bool = False) -> np.ndarray:
     """Explicit boolean mask A[2L, 2L] over (query, key) positions.
 
     Rows/cols 0..L-1 are the clean copy, L..2L-1 the corrupted copy.  Built
-    from the block ids by broadcasting the four cases of `allowed`.
+    from the block ids (and positions) by broadcasting the cases of `allowed`.
     """
     if L % M != 0:
         raise ValueError("L must be a multiple of the block size M")
-    b = np.arange(L) // M
+    pos = np.arange(L)
+    b = pos // M
     bq, bk = b[:, None], b[None, :]
     A = np.zeros((2 * L, 2 * L), dtype=bool)
-    A[:L, :L] = bk <= bq          # clean q, clean k
+    if clean_causal:
+        A[:L, :L] = pos[None, :] <= pos[:, None]   # clean q, clean k (token-causal)
+    else:
+        A[:L, :L] = bk <= bq                        # clean q, clean k (block-causal)
     A[:L, L:] = False             # clean q, corrupted k
     A[L:, :L] = bk < bq           # corrupted q, clean k
     A[L:, L:] = bk == bq          # corrupted q, corrupted k
+    if window > 0:
+        near = (pos[:, None] - pos[None, :]) < window
+        A &= np.tile(near, (2, 2))
     return A
 
 
-def mask_row(q_stream: int, i: int, L: int, M: int) -> np.ndarray:
+def mask_row(q_stream: int, i: int, L: int, M: int, window: int = 0,
+             clean_causal: bool = False) -> np.ndarray:
     """Row (q_stream, i) of `bd_mask`, length 2L (clean keys then corrupted)."""
-    b = np.arange(L) // M
+    pos = np.arange(L)
+    b = pos // M
     bi = i // M
     row = np.zeros(2 * L, dtype=bool)
     if q_stream == CLEAN:
-        row[:L] = b <= bi
+        row[:L] = (pos <= i) if clean_causal else (b <= bi)
     else:
         row[:L] = b < bi
         row[L:] = b == bi
+    if window > 0:
+        near = (i - pos) < window
+        row[:L] &= near
+        row[L:] &= near
     return row
 
 
@@ -167,7 +191,7 @@ def _stack_streams(x_clean, x_corr):
                            np.asarray(x_corr, np.float64)], axis=0)
 
 
-def bd_attention_fwd(qc, kc, vc, qx, kx, vx, M, scale):
+def bd_attention_fwd(qc, kc, vc, qx, kx, vx, M, scale, window=0, clean_causal=False):
     """Full forward of two-copy block-diffusion attention.
 
     Inputs [L, H, d] (H = Hq for q, Hkv for k/v); qc may be None for the
@@ -178,7 +202,7 @@ def bd_attention_fwd(qc, kc, vc, qx, kx, vx, M, scale):
     L, Hkv, d = np.shape(kc)
     Hq = np.shape(qx)[1]
     G = Hq // Hkv
-    A = bd_mask(L, M)
+    A = bd_mask(L, M, window, clean_causal)
     K = _stack_streams(kc, kx)
     V = _stack_streams(vc, vx)
     has_clean = qc is not None
@@ -197,7 +221,7 @@ def bd_attention_fwd(qc, kc, vc, qx, kx, vx, M, scale):
     return Oc, Ox, lse
 
 
-def bd_attention_bwd(qc, kc, vc, qx, kx, vx, doc, dox, M, scale):
+def bd_attention_bwd(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, window=0, clean_causal=False):
     """Analytic backward of `bd_attention_fwd`.
 
     Returns dict with dq_clean, dq_corr, dk_clean, dv_clean, dk_corr, dv_corr
@@ -209,7 +233,7 @@ def bd_attention_bwd(qc, kc, vc, qx, kx, vx, doc, dox, M, scale):
     L, Hkv, d = np.shape(kc)
     Hq = np.shape(qx)[1]
     G = Hq // Hkv
-    A = bd_mask(L, M)
+    A = bd_mask(L, M, window, clean_causal)
     K = _stack_streams(kc, kx)
     V = _stack_streams(vc, vx)
     has_clean = qc is not None
@@ -352,7 +376,7 @@ def key_parts(L: int, P: int) -> np.ndarray:
     return part
 
 
-def bd_attention_fwd_sharded(qc, kc, vc, qx, kx, vx, M, scale, P):
+def bd_attention_fwd_sharded(qc, kc, vc, qx, kx, vx, M, scale, P, window=0, clean_causal=False):
     """Forward via P+1 partials per query row and the LSE merge.
 
     Returns (Oc, Ox, lse, partials) where partials = (o_parts [P+1,2,L,Hq,d],
@@ -362,7 +386,7 @@ def bd_attention_fwd_sharded(qc, kc, vc, qx, kx, vx, M, scale, P):
     L, Hkv, d = np.shape(kc)
     Hq = np.shape(qx)[1]
     G = Hq // Hkv
-    A = bd_mask(L, M)
+    A = bd_mask(L, M, window, clean_causal)
     K = _stack_streams(kc, kx)
     V = _stack_streams(vc, vx)
     part = key_parts(L, P)
@@ -398,7 +422,7 @@ def bd_attention_fwd_sharded(qc, kc, vc, qx, kx, vx, M, scale, P):
 # --------------------------------------------------------------------------
 # Tile schedule derived from the mask
 # --------------------------------------------------------------------------
-def tile_pairs(L, M, Tq, Tkv, P=1, has_clean_queries=True):
+def tile_pairs(L, M, Tq, Tkv, P=1, has_clean_queries=True, window=0, clean_causal=False):
     """Set of (q_stream, q_tile, kv_stream, kv_tile, full, part) over every
     (query-tile, key-tile) pair holding at least one allowed entry.
 
@@ -408,7 +432,7 @@ def tile_pairs(L, M, Tq, Tkv, P=1, has_clean_queries=True):
     """
     if (L // (2 * P)) % Tkv != 0 and P > 1:
         raise ValueError("Tkv must divide L/(2P)")
-    A = bd_mask(L, M)
+    A = bd_mask(L, M, window, clean_causal)
     if P == 1:
         part = np.concatenate([np.zeros(L, np.int32), np.ones(L, np.int32)])
     else:
@@ -445,7 +469,8 @@ def _gather_rows(qc, qx, doc, dox, rows, h):
     return q, do
 
 
-def sampled_rows(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples):
+def sampled_rows(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples, window=0,
+                 clean_causal=False):
     """Exact O, lse, D and dQ for sampled query rows.
 
     samples: iterable of (q_stream, i, h).  Each row depends only on itself,
@@ -469,7 +494,7 @@ def sampled_rows(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples):
         for h in heads:
             rows = by_head[h]
             q, do = _gather_rows(qc, qx, doc, dox, rows, h)
-            allow = np.stack([mask_row(qs, i, L, M) for qs, i in rows])
+            allow = np.stack([mask_row(qs, i, L, M, window, clean_causal) for qs, i in rows])
             o, z = masked_attention(q, K, V, allow, scale)
             dq, _, _, D = masked_attention_bwd(q, K, V, allow, scale, do)
             for r, (qs, i) in enumerate(rows):
@@ -478,7 +503,7 @@ def sampled_rows(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples):
     return out
 
 
-def readers_of_key(k_stream, j, L, M, has_clean_queries=True):
+def readers_of_key(k_stream, j, L, M, has_clean_queries=True, window=0, clean_causal=False):
     """All query rows (q_stream, i) whose mask row allows key (k_stream, j)."""
     bj = j // M
     out = []
@@ -488,10 +513,13 @@ def readers_of_key(k_stream, j, L, M, has_clean_queries=True):
         if has_clean_queries:
             out += [(CLEAN, i) for i in range(bj * M, L)]
         out += [(CORR, i) for i in range((bj + 1) * M, L)]
+    if window > 0 or clean_causal:  # the block rules above give a superset
+        out = [(qs, i) for qs, i in out if allowed(qs, i, k_stream, j, M, window, clean_causal)]
     return out
 
 
-def sampled_keys(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples):
+def sampled_keys(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples, window=0,
+                 clean_causal=False):
     """Exact dK, dV for sampled keys (k_stream, j, g).
 
     dK_j and dV_j sum over every query row that reads key j, over the G query
@@ -510,13 +538,14 @@ def sampled_keys(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples):
         by_g.setdefault(g, []).append((ks, j))
     out = {}
     for g, keys in by_g.items():
-        readers = sorted({r for ks, j in keys for r in readers_of_key(ks, j, L, M, has_clean)})
+        readers = sorted({r for ks, j in keys
+                          for r in readers_of_key(ks, j, L, M, has_clean, window, clean_causal)})
         K, V = _kv_of_head(kc, kx, vc, vx, g)
         dk = np.zeros((len(keys), d))
         dv = np.zeros((len(keys), d))
         cols = [ks * L + j for ks, j in keys]
         if readers:
-            allow = np.stack([mask_row(qs, i, L, M) for qs, i in readers])
+            allow = np.stack([mask_row(qs, i, L, M, window, clean_causal) for qs, i in readers])
             for h in range(g * G, (g + 1) * G):
                 q, do = _gather_rows(qc, qx, doc, dox, readers, h)
                 _, dk_all, dv_all, _ = masked_attention_bwd(q, K, V, allow, scale, do)
@@ -533,9 +562,20 @@ def sampled_keys(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples):
 # ([Blog] "CSBP：BP 管损坏块，CP 管干净上下文": CP and CSBP compute the same legal
 #  pairs, Theta(L^2) in total)
 # --------------------------------------------------------------------------
-def allowed_pairs_per_head(L, M, has_clean_queries=True):
+def allowed_pairs_per_head(L, M, has_clean_queries=True, window=0, clean_causal=False):
     """Number of allowed (query, key) pairs for one query head."""
     B = L // M
-    corr = sum(M * (M + b * M) for b in range(B))
-    clean = sum(M * ((b + 1) * M) for b in range(B)) if has_clean_queries else 0
-    return corr + clean
+    if window <= 0 and not clean_causal:
+        corr = sum(M * (M + b * M) for b in range(B))
+        clean = sum(M * ((b + 1) * M) for b in range(B)) if has_clean_queries else 0
+        return corr + clean
+    # per query row, each key set is one range of positions [lo, hi)
+    i = np.arange(L, dtype=np.int64)
+    b = i // M
+    w_lo = np.maximum(0, i - window + 1) if window > 0 else np.zeros(L, np.int64)
+    n = np.maximum(0, b * M - w_lo)                                   # corrupted q, clean k
+    n += np.maximum(0, (b + 1) * M - np.maximum(b * M, w_lo))         # corrupted q, own block
+    if has_clean_queries:
+        hi = (i + 1) if clean_causal else (b + 1) * M
+        n += np.maximum(0, hi - w_lo)                                 # clean q, clean k
+    return int(n.sum())

@@ -38,7 +38,8 @@ def run_gpu(w: Workload, L=None, seed=None, P=None):
     t = make_inputs(w, "cuda", seed=seed, L=L)
     attn = csbp.BlockDiffusionAttention(w.batch, L, w.M, w.Hq, w.Hkv, w.d,
                                         P=w.P if P is None else P,
-                                        has_clean_queries=w.has_clean_queries)
+                                        has_clean_queries=w.has_clean_queries,
+                                        window=w.window, clean_causal=w.clean_causal)
     out = attn.forward(t)
     g = attn.backward(t, out)
     attn.check()
@@ -59,6 +60,15 @@ SMALL = [
     Workload("sharded_small", 1, 1024, 16, 4, 2, 128, P=2, seed=19),
     Workload("sharded_p4", 1, 2048, 32, 2, 1, 128, P=4, seed=20),
     Workload("drafter_sharded", 1, 1024, 16, 2, 1, 64, P=2, has_clean_queries=False, seed=21),
+    # sliding window (keys less than W positions back) and token-causal clean queries
+    Workload("win_gqa", 1, 512, 16, 4, 2, 128, window=100, seed=22),
+    Workload("causal_clean", 1, 384, 32, 2, 1, 128, clean_causal=True, seed=23),
+    Workload("win_causal_ragged", 1, 400, 16, 4, 2, 64, window=150, clean_causal=True, seed=24),
+    Workload("win_sharded", 1, 1024, 16, 4, 2, 128, P=2, window=200, seed=25),
+    Workload("win_drafter", 1, 512, 16, 4, 1, 128, has_clean_queries=False, window=64, seed=26),
+    Workload("win_one", 1, 256, 8, 2, 1, 128, window=1, clean_causal=True, seed=27),
+    Workload("win_tokens", 1, 256, 1, 2, 2, 64, window=37, seed=28),
+    Workload("win_tile_multiple", 1, 1024, 32, 2, 1, 128, window=256, clean_causal=True, seed=29),
 ]
 
 
@@ -68,9 +78,11 @@ def test_small_cases_match_oracle_elementwise(w):
     for b in range(w.batch):
         f = {k: (to_f64(v[b]) if v is not None else None) for k, v in t.items()}
         Oc, Ox, Z = O.bd_attention_fwd(f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"],
-                                       f["k_corr"], f["v_corr"], w.M, w.scale)
+                                       f["k_corr"], f["v_corr"], w.M, w.scale, w.window,
+                                       w.clean_causal)
         G = O.bd_attention_bwd(f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"],
-                               f["k_corr"], f["v_corr"], f["do_clean"], f["do_corr"], w.M, w.scale)
+                               f["k_corr"], f["v_corr"], f["do_clean"], f["do_corr"], w.M, w.scale,
+                               w.window, w.clean_causal)
         gl = to_f64(lse[b])
         assert np.abs(to_f64(ox[b]) - Ox).max() <= TOL_O
         assert np.abs(gl[1] - Z[1]).max() <= TOL_LSE
@@ -168,7 +180,8 @@ def _sampled_check(w, t, out, g, rows_per_head, n_keys, seed):
         for _ in range(rows_per_head):
             samples.append((int(rng.choice(streams)), int(rng.integers(0, L)), h))
     ref = O.sampled_rows(fv["q_clean"], fv["k_clean"], fv["v_clean"], fv["q_corr"], fv["k_corr"],
-                         fv["v_corr"], fv["do_clean"], fv["do_corr"], w.M, w.scale, samples)
+                         fv["v_corr"], fv["do_clean"], fv["do_corr"], w.M, w.scale, samples,
+                         w.window, w.clean_causal)
     o_err, z_err = 0.0, 0.0
     dq_got, dq_want = [], []
     for (qs, i, h), (o, z, D, dq) in ref.items():
@@ -187,7 +200,8 @@ def _sampled_check(w, t, out, g, rows_per_head, n_keys, seed):
         keys.append((1, int(rng.integers(0, L)), g_))
         keys.append((0, int(rng.integers(L - 2 * w.M, L - w.M)), g_))
     kref = O.sampled_keys(fv["q_clean"], fv["k_clean"], fv["v_clean"], fv["q_corr"], fv["k_corr"],
-                          fv["v_corr"], fv["do_clean"], fv["do_corr"], w.M, w.scale, keys)
+                          fv["v_corr"], fv["do_clean"], fv["do_corr"], w.M, w.scale, keys,
+                          w.window, w.clean_causal)
     got_k, want_k, got_v, want_v = [], [], [], []
     for (ks, j, gg), (dk, dv) in kref.items():
         sfx = "clean" if ks == 0 else "corr"
@@ -200,7 +214,8 @@ def _sampled_check(w, t, out, g, rows_per_head, n_keys, seed):
 
 
 @pytest.mark.parametrize("name,rows,keys,seed", [("dense14b", 256, 8, 101), ("sharded", 16, 4, 102),
-                                                  ("long", 8, 4, 103), ("drafter", 2, 2, 104)])
+                                                  ("long", 8, 4, 103), ("drafter", 2, 2, 104),
+                                                  ("window1k", 64, 8, 105)])
 def test_full_size_workloads_sampled(name, rows, keys, seed):
     w = WORKLOADS[name]
     t, out, g = run_gpu(w)

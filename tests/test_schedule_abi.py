@@ -72,14 +72,25 @@ SWEEP = [
     (512, 16, 32, 2, False), (200, 8, 32, 1, True), (384, 128, 128, 1, True),
     (1024, 64, 128, 1, True), (1024, 32, 128, 4, True), (1040, 16, 128, 1, True),
 ]
+SWEEP = [s + (0, False) for s in SWEEP] + [
+    # L, M, T, P, has_clean, window, token-causal clean
+    (256, 16, 32, 1, True, 0, True), (480, 16, 32, 1, True, 0, True),
+    (256, 16, 32, 1, True, 40, False), (256, 16, 32, 1, True, 33, True),
+    (512, 16, 32, 2, True, 100, False), (512, 8, 32, 4, True, 64, True),
+    (480, 32, 32, 1, False, 50, False), (256, 64, 32, 1, True, 1, False),
+    (256, 1, 32, 1, True, 17, True), (1040, 16, 128, 1, True, 300, True),
+    (1024, 64, 128, 1, True, 128, False), (1024, 32, 128, 4, True, 129, False),
+    (384, 128, 128, 1, True, 1000, True),
+]
 
 
-@pytest.mark.parametrize("L,M,T,P,clean", SWEEP)
-def test_schedule_matches_oracle_tile_set_bit_exactly(L, M, T, P, clean):
-    prob = csbp.make_problem(1, L, M, 2, 1, 64, P=P, has_clean_queries=clean, tile=T)
+@pytest.mark.parametrize("L,M,T,P,clean,W,causal", SWEEP)
+def test_schedule_matches_oracle_tile_set_bit_exactly(L, M, T, P, clean, W, causal):
+    prob = csbp.make_problem(1, L, M, 2, 1, 64, P=P, has_clean_queries=clean, tile=T,
+                             window=W, clean_causal=causal)
     bo, co, words, info = csbp.block_schedule(prob)
     fwd, bwd, fc, bc = expand(words, info, P)
-    want = O.tile_pairs(L, M, T, T, P, clean)
+    want = O.tile_pairs(L, M, T, T, P, clean, W, causal)
     if P == 1:
         got_fwd = {x[:5] + ((1 if x[2] == 1 else 0),) for x in fwd}
         assert all(x[5] == -1 for x in fwd)
@@ -142,6 +153,19 @@ def test_drafter_schedule_count():
     assert info.n_bwd_tasks == 2 * nT
 
 
+def test_windowed_full_size_schedule_count():
+    """L = 16384, M = 32, window 1024 = 8 key tiles: query tile t of either
+    copy touches clean key tiles max(0, t-8) .. t, and corrupted query tiles
+    their own corrupted tile as well."""
+    w = WORKLOADS["window1k"]
+    prob = csbp.make_problem(w.batch, w.L, w.M, w.Hq, w.Hkv, w.d, window=w.window)
+    _, _, _, info = csbp.block_schedule(prob)
+    nT, wt = w.L // 128, w.window // 128
+    per_stream = sum(min(t + 1, wt + 1) for t in range(nT))
+    assert info.tile_pairs == 2 * per_stream + nT
+    assert info.n_bwd_tasks == 2 * nT
+
+
 @pytest.mark.parametrize("field,value,code", [
     ("M", 3, -1),            # L % M != 0
     ("Hkv", 3, -1),          # Hq % Hkv != 0
@@ -150,6 +174,8 @@ def test_drafter_schedule_count():
     ("scale", 0.0, -1),
     ("L", 0, -1),
     ("has_clean_queries", 2, -1),
+    ("window", -1, -1),
+    ("clean_causal", 2, -1),
 ])
 def test_schedule_rejects_invalid_problems(field, value, code):
     prob = csbp.make_problem(1, 1024, 64, 4, 2, 64)
