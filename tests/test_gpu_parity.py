@@ -89,13 +89,16 @@ def test_small_cases_match_oracle_elementwise(w):
         if w.has_clean_queries:
             assert np.abs(to_f64(oc[b]) - Oc).max() <= TOL_O
             assert np.abs(gl[0] - Z[0]).max() <= TOL_LSE
-            assert rel_fro(to_f64(g["dq_clean"][b]), G["dq_clean"]) <= TOL_REL
-        assert rel_fro(to_f64(g["dq_corr"][b]), G["dq_corr"]) <= TOL_REL
-        for k in ("dk_clean", "dv_clean", "dk_corr", "dv_corr"):
+        names = ["dq_corr", "dk_clean", "dv_clean", "dk_corr", "dv_corr"]
+        if w.has_clean_queries:
+            names.append("dq_clean")
+        for k in names:
             want = G[k]
             got = to_f64(g[k][b])
             if np.linalg.norm(want) == 0:
-                assert np.abs(got).max() == 0, k
+                # an exactly cancelling gradient (a row or key with one
+                # partner: dS = P (dP - D) = 0) leaves only rounding residue
+                assert np.abs(got).max() <= TOL_O, k
             else:
                 assert rel_fro(got, want) <= TOL_REL, (k, rel_fro(got, want))
 
