@@ -94,6 +94,11 @@ WORKLOADS = {
                         has_clean_queries=False, seed=1238),
     # sliding-window layer: the dense shapes with a 1,024-token window
     "window1k": Workload("window1k", 1, 16384, 32, 40, 8, 128, window=1024, seed=1239),
+    # the dense shapes at the larger block sizes of the pages' training recipes
+    "block128": Workload("block128", 1, 16384, 128, 40, 8, 128, seed=1240),
+    "block256": Workload("block256", 1, 16384, 256, 40, 8, 128, seed=1241),
+    "block512": Workload("block512", 1, 16384, 512, 40, 8, 128, seed=1242),
+    "block1024": Workload("block1024", 1, 16384, 1024, 40, 8, 128, seed=1243),
 }
 
 

@@ -69,6 +69,10 @@ SMALL = [
     Workload("win_one", 1, 256, 8, 2, 1, 128, window=1, clean_causal=True, seed=27),
     Workload("win_tokens", 1, 256, 1, 2, 2, 64, window=37, seed=28),
     Workload("win_tile_multiple", 1, 1024, 32, 2, 1, 128, window=256, clean_causal=True, seed=29),
+    # blocks spanning several tiles
+    Workload("block512_small", 1, 1536, 512, 2, 1, 128, seed=34),
+    Workload("block1024_gqa", 1, 2048, 1024, 4, 2, 64, seed=35),
+    Workload("block384_ragged_tiles", 1, 1152, 384, 2, 2, 128, seed=36),
 ]
 
 
@@ -218,7 +222,8 @@ def _sampled_check(w, t, out, g, rows_per_head, n_keys, seed):
 
 @pytest.mark.parametrize("name,rows,keys,seed", [("dense14b", 256, 8, 101), ("sharded", 16, 4, 102),
                                                   ("long", 8, 4, 103), ("drafter", 2, 2, 104),
-                                                  ("window1k", 64, 8, 105)])
+                                                  ("window1k", 64, 8, 105),
+                                                  ("block1024", 32, 8, 106)])
 def test_full_size_workloads_sampled(name, rows, keys, seed):
     w = WORKLOADS[name]
     t, out, g = run_gpu(w)
