@@ -232,11 +232,190 @@ def launches_per_step(w):
     return fwd + bwd
 
 
+# ------------------------------------------------------- vocabulary loss
+CE_METRIC = ("TFLOP/s streamed LM-head cross-entropy, loss + dH (+ dW for a trained head) "
+             "(1 GB300) and % of BF16 peak")
+CE_KINDS = {2: "logits_gemm", 3: "row_kernel", 4: "dh_gemm", 5: "dw_gemm"}
+
+
+def ce_cpu_oracle_sample(w, seconds, seed=7):
+    """The float64 oracle on seeded sample rows of the workload for about
+    `seconds`: each row's logits over the whole vocabulary, its LSE, loss
+    and dH (4 V Dm FLOPs per row; dW needs every row and is not sampled)."""
+    import numpy as np
+    import torch
+
+    from block_diffusion_lm_gb300.inputs import make_ce_inputs
+    from oracle import vocab_ce_oracle as C
+
+    x = make_ce_inputs(w, "cpu")
+    W = x["w"].to(torch.float64).numpy()
+    H = x["h"]
+    t = x["target"].numpy()
+    rng = np.random.default_rng(seed)
+    rows_done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        rows = rng.choice(w.N, size=8, replace=False)
+        C.vocab_ce_rows(H[torch.as_tensor(rows)].to(torch.float64).numpy(), W, t[rows],
+                        x["grad_scale"], np.arange(8))
+        rows_done += 8
+    dt = time.perf_counter() - t0
+    value = rows_done * 4.0 * w.V * w.Dm / dt / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{rows_done} seeded rows (logits over V={w.V}, LSE, loss, dH; "
+                      f"4*V*Dm FLOPs each), {dt:.1f} s",
+            "extrapolated_step_s": w.flops() / (value * 1e12)}
+
+
+def bench_ce(args, w, rank, world, local):
+    config = {"workload": w.name, "rows": w.N, "d_model": w.Dm, "vocab": w.V,
+              "chunk_rows": w.chunk, "head_grad": w.head_grad,
+              "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single"}
+    flops = w.flops()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = [ce_cpu_oracle_sample(w, max(2.0, args.cpu_seconds / max(args.steps, 1)))
+                 for _ in range(args.steps)]
+        v = statistics.median(s["value"] for s in steps)
+        print(json.dumps({
+            "impl": "reference", "metric": CE_METRIC, "value": v, "unit": "TFLOP/s",
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": flops / (v * 1e12) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config,
+            "cpu_baseline": dict(steps[0], value=v),
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from block_diffusion_lm_gb300 import build, csbp
+    from block_diffusion_lm_gb300.inputs import make_ce_inputs
+
+    build.build()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    x = make_ce_inputs(w, dev)
+    ce = csbp.VocabCrossEntropy(w.N, w.Dm, w.V, w.chunk, w.head_grad, x["grad_scale"],
+                                device=dev)
+    out = ce.alloc_outputs()
+    n_chunks = -(-w.N // (w.chunk if w.chunk > 0 else 8192))
+    in_bytes = sum(v.numel() * v.element_size() for v in (x["h"], x["w"], x["target"]))
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            ce(x["h"], x["w"], x["target"], out, stream=stream)
+    ce.check(stream)
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    csbp.kernel_timing(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            ce(x["h"], x["w"], x["target"], out, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    csbp.kernel_timing(False)
+    ce.check(stream)
+    total_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    if world > 1:
+        dist.barrier()
+    ms_per_step = total_ms / args.steps
+    value = whole_job_tflops(world, flops, ms_per_step)
+
+    kernels = {}
+    for kind, name in CE_KINDS.items():
+        ms, n = csbp.kernel_timing_read_kind(kind)
+        if n:
+            kernels[name] = {"ms_per_step": ms / args.steps, "launches": n,
+                             "avg_launch_ms": ms / n}
+    gemm_flops = 2.0 * w.N * w.V * w.Dm
+    for name in ("logits_gemm", "dh_gemm", "dw_gemm"):
+        if name in kernels:
+            kernels[name]["tflops"] = gemm_flops / (kernels[name]["ms_per_step"] * 1e-3) / 1e12
+    if "row_kernel" in kernels:
+        row_bytes = w.N * w.V * 6.0  # fp32 logits in, bf16 g out
+        kernels["row_kernel"]["gbs"] = row_bytes / (kernels["row_kernel"]["ms_per_step"] * 1e-3) / 1e9
+    top = max((k for k in kernels if k.endswith("gemm")), key=lambda k: kernels[k]["ms_per_step"])
+    pk = peaks()
+    peak = pk["bf16_sustained"]
+    top_launch_flops = gemm_flops / n_chunks
+    achieved = top_launch_flops / (kernels[top]["avg_launch_ms"] * 1e-3) / 1e12
+
+    # end to end: pinned host inputs up, loss/LSE/dH(/dW) down, every step
+    host = {k: x[k].cpu().pin_memory() for k in ("h", "w", "target")}
+    dev_in = {k: torch.empty_like(x[k]) for k in host}
+    res = [r for r in out if r is not None]
+    host_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res]
+    out_bytes = sum(r.numel() * r.element_size() for r in res)
+    e2e_steps = max(3, min(args.steps, 10))
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        f0.record(stream)
+        for _ in range(e2e_steps):
+            for k, v in host.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            ce(dev_in["h"], dev_in["w"], dev_in["target"], out, stream=stream)
+            for r, hbuf in zip(res, host_out):
+                hbuf.copy_(r, non_blocking=True)
+        f1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, dev)
+    e2e = {"value": whole_job_tflops(world, flops, e2e_ms), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+           "overlap": "none (copies and compute in order on one stream)"}
+
+    line = {
+        "metric": CE_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(config, l2=f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB resident "
+                                  f"vs {L2_BYTES / 2**20:.0f} MiB L2); no flush"),
+        "pct_of_bf16_peak": value / world / peak,
+        "kernels": kernels,
+        "roofline": {"bound": "tensor", "kernel": f"ce_gemm_kernel ({top})",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "peak_source": f"bf16_tflops_sustained of {pk['source']}",
+                     "launch_ms": kernels[top]["avg_launch_ms"],
+                     "launches_timed": kernels[top]["launches"], "traffic": None},
+        "e2e": e2e,
+        "gpu_launches": n_chunks * (4 if w.head_grad else 3) * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = ce_cpu_oracle_sample(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from block_diffusion_lm_gb300.inputs import CE_WORKLOADS
+    if args.config in CE_WORKLOADS:
+        bench_ce(args, CE_WORKLOADS[args.config], rank, world, local)
+        return
 
     import dataclasses
 

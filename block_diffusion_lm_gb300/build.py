@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcsbp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["schedule.cpp", "csbp_api.cu", "attn_fwd.cu", "attn_bwd.cu", "elementwise.cu",
-           "noalloc.cu"]
+           "noalloc.cu", "vocab_ce.cu"]
 
 
 def nvcc() -> str:
@@ -32,7 +32,7 @@ def nvcc() -> str:
 
 
 def _headers_mtime() -> float:
-    hs = [os.path.join(INCLUDE, "csbp.h")]
+    hs = [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     hs += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     return max(os.path.getmtime(h) for h in hs)
 

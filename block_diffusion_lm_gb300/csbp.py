@@ -15,7 +15,8 @@ import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libcsbp.so")
-HEADER = os.path.join(os.path.dirname(_PKG), "include", "csbp.h")
+INCLUDE = os.path.join(os.path.dirname(_PKG), "include")
+HEADER = os.path.join(INCLUDE, "csbp.h")
 
 OK = 0
 STATUS = {0: "CSBP_OK", -1: "CSBP_ERR_INVALID", -2: "CSBP_ERR_UNSUPPORTED",
@@ -40,6 +41,12 @@ class Problem(ctypes.Structure):
 class Inputs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")]
+
+
+class CeProblem(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("d_model", ctypes.c_int32), ("vocab", ctypes.c_int32),
+                ("chunk_rows", ctypes.c_int32), ("head_grad", ctypes.c_int32),
+                ("grad_scale", ctypes.c_float)]
 
 
 class ScheduleInfo(ctypes.Structure):
@@ -78,18 +85,27 @@ def lib():
         L.csbp_kernel_timing.argtypes = [i32]
         L.csbp_kernel_timing_read.argtypes = [P(ctypes.c_double), P(i32), P(ctypes.c_double),
                                               P(i32)]
+        L.csbp_kernel_timing_read_kind.argtypes = [i32, P(ctypes.c_double), P(i32)]
+        L.csbp_ce_workspace_bytes.argtypes = [P(CeProblem)]
+        L.csbp_ce_workspace_bytes.restype = sz
+        L.csbp_vocab_ce.argtypes = [P(CeProblem), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         for fn in ("csbp_block_schedule", "csbp_attn_fwd", "csbp_attn_bwd", "csbp_lse_merge",
-                   "csbp_check_status", "csbp_kernel_timing", "csbp_kernel_timing_read"):
+                   "csbp_check_status", "csbp_kernel_timing", "csbp_kernel_timing_read",
+                   "csbp_kernel_timing_read_kind", "csbp_vocab_ce"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
 
 
 def header_functions():
-    """Names of the functions include/csbp.h declares."""
-    with open(HEADER) as f:
-        text = f.read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(csbp_\w+)\s*\(", text, re.M)))
+    """Names of the functions the headers under include/ declare."""
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            with open(os.path.join(INCLUDE, h)) as f:
+                text = f.read()
+            names.update(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(csbp_\w+)\s*\(", text, re.M))
+    return sorted(names)
 
 
 def _check(fn, status):
@@ -139,6 +155,15 @@ def kernel_timing_read():
            lib().csbp_kernel_timing_read(ctypes.byref(fm), ctypes.byref(fn), ctypes.byref(bm),
                                          ctypes.byref(bn)))
     return fm.value, fn.value, bm.value, bn.value
+
+
+def kernel_timing_read_kind(kind: int):
+    """(ms, launches) of one timer kind: 0 fwd, 1 bwd, 2 CE logits GEMM,
+    3 CE row kernel, 4 CE dH GEMM, 5 CE dW GEMM."""
+    ms, n = ctypes.c_double(), ctypes.c_int32()
+    _check("csbp_kernel_timing_read_kind",
+           lib().csbp_kernel_timing_read_kind(kind, ctypes.byref(ms), ctypes.byref(n)))
+    return ms.value, n.value
 
 
 def workspace_bytes(problem: Problem, which: int) -> int:
@@ -268,3 +293,57 @@ class BlockDiffusionAttention:
     def check(self, stream=None):
         check_status(self.ws_fwd, stream)
         check_status(self.ws_bwd, stream)
+
+
+# ------------------------------------------------------------ vocabulary loss
+def make_ce_problem(rows, d_model, vocab, chunk_rows=0, head_grad=True, grad_scale=1.0):
+    return CeProblem(int(rows), int(d_model), int(vocab), int(chunk_rows),
+                     1 if head_grad else 0, float(grad_scale))
+
+
+def ce_workspace_bytes(problem: CeProblem) -> int:
+    return int(lib().csbp_ce_workspace_bytes(ctypes.byref(problem)))
+
+
+def vocab_ce(problem, h, w, target, loss, lse, dh, dw, workspace, stream=None):
+    st = lib().csbp_vocab_ce(ctypes.byref(problem), _ptr(h), _ptr(w), _ptr(target), _ptr(loss),
+                             _ptr(lse), _ptr(dh), _ptr(dw), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check("csbp_vocab_ce", st)
+
+
+class VocabCrossEntropy:
+    """Owns the workspace of one LM-head cross-entropy shape.
+
+    __call__(h, w, target) takes bf16 h [N, Dm], bf16 w [V, Dm] and int32
+    target [N] on the GPU and returns (loss [N], lse [N], dh [N, Dm] bf16,
+    dw [V, Dm] fp32 or None for a frozen head).
+    """
+
+    def __init__(self, rows, d_model, vocab, chunk_rows=0, head_grad=True, grad_scale=1.0,
+                 device="cuda"):
+        import torch
+        self.problem = make_ce_problem(rows, d_model, vocab, chunk_rows, head_grad, grad_scale)
+        n = ce_workspace_bytes(self.problem)
+        if n == 0:
+            raise CsbpError("csbp_ce_workspace_bytes", -1)
+        self.ws = torch.zeros(n, dtype=torch.uint8, device=device)
+        self.device = device
+
+    def alloc_outputs(self):
+        import torch
+        p = self.problem
+        loss = torch.empty(p.rows, dtype=torch.float32, device=self.device)
+        lse = torch.empty(p.rows, dtype=torch.float32, device=self.device)
+        dh = torch.empty((p.rows, p.d_model), dtype=torch.bfloat16, device=self.device)
+        dw = (torch.empty((p.vocab, p.d_model), dtype=torch.float32, device=self.device)
+              if p.head_grad else None)
+        return loss, lse, dh, dw
+
+    def __call__(self, h, w, target, out=None, stream=None):
+        loss, lse, dh, dw = out if out is not None else self.alloc_outputs()
+        vocab_ce(self.problem, h, w, target, loss, lse, dh, dw, self.ws, stream)
+        return loss, lse, dh, dw
+
+    def check(self, stream=None):
+        check_status(self.ws, stream)

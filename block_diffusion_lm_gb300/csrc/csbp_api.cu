@@ -160,32 +160,47 @@ struct KernelTimer {
   bool on = false;
   int device = -1;
   std::vector<cudaEvent_t> start, stop;
-  std::vector<int> kind;  // 0 fwd, 1 bwd, per recorded pair
+  std::vector<int> kind;  // timer kind of each recorded pair (see csbp.h)
 };
 KernelTimer& timer() {
   static KernelTimer t;
   return t;
 }
 
-// Returns the pair index to record, or -1.
-int timer_begin(int kind, cudaStream_t stream) {
+}  // namespace
+
+int timer_begin(int kind, void* stream) {
   KernelTimer& t = timer();
   std::lock_guard<std::mutex> lk(t.mu);
   if (!t.on || static_cast<int>(t.kind.size()) >= KernelTimer::kCap) return -1;
   const int i = static_cast<int>(t.kind.size());
-  if (cudaEventRecord(t.start[i], stream) != cudaSuccess) return -1;
+  if (cudaEventRecord(t.start[i], static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
   t.kind.push_back(kind);
   return i;
 }
 
-void timer_end(int i, cudaStream_t stream) {
+void timer_end(int i, void* stream) {
   if (i < 0) return;
   KernelTimer& t = timer();
   std::lock_guard<std::mutex> lk(t.mu);
-  cudaEventRecord(t.stop[i], stream);
+  cudaEventRecord(t.stop[i], static_cast<cudaStream_t>(stream));
 }
 
-}  // namespace
+bool encode_map_2d(void* map, bool f32, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(static_cast<CUtensorMap*>(map),
+                   f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 }  // namespace csbp
 
@@ -225,6 +240,7 @@ extern "C" csbp_status csbp_kernel_timing_read(double* fwd_ms, int32_t* n_fwd, d
   double ms[2] = {0.0, 0.0};
   int32_t n[2] = {0, 0};
   for (size_t i = 0; i < t.kind.size(); ++i) {
+    if (t.kind[i] > 1) continue;
     float e = 0.f;
     if (cudaEventSynchronize(t.stop[i]) != cudaSuccess ||
         cudaEventElapsedTime(&e, t.start[i], t.stop[i]) != cudaSuccess)
@@ -236,6 +252,26 @@ extern "C" csbp_status csbp_kernel_timing_read(double* fwd_ms, int32_t* n_fwd, d
   if (n_fwd) *n_fwd = n[0];
   if (bwd_ms) *bwd_ms = ms[1];
   if (n_bwd) *n_bwd = n[1];
+  return CSBP_OK;
+}
+
+extern "C" csbp_status csbp_kernel_timing_read_kind(int32_t kind, double* ms, int32_t* n) {
+  if (kind < 0 || kind >= kTimerKinds) return CSBP_ERR_INVALID;
+  KernelTimer& t = timer();
+  std::lock_guard<std::mutex> lk(t.mu);
+  double sum = 0.0;
+  int32_t cnt = 0;
+  for (size_t i = 0; i < t.kind.size(); ++i) {
+    if (t.kind[i] != kind) continue;
+    float e = 0.f;
+    if (cudaEventSynchronize(t.stop[i]) != cudaSuccess ||
+        cudaEventElapsedTime(&e, t.start[i], t.stop[i]) != cudaSuccess)
+      return CSBP_ERR_CUDA;
+    sum += e;
+    ++cnt;
+  }
+  if (ms) *ms = sum;
+  if (n) *n = cnt;
   return CSBP_OK;
 }
 

@@ -23,6 +23,20 @@ enum HeaderWord {
 };
 
 csbp_status validate_problem(const csbp_problem* p);
+
+// Kernel timing (csbp_kernel_timing): kinds 0 fwd, 1 bwd, 2 CE logits GEMM,
+// 3 CE row kernel, 4 CE dH GEMM, 5 CE dW GEMM.  timer_begin returns the pair
+// index to close with timer_end, or -1 when not recording.
+constexpr int kTimerKinds = 6;
+int timer_begin(int kind, void* stream);
+void timer_end(int i, void* stream);
+
+// Encode a 2-D TMA descriptor (a CUtensorMap at `map`) over a row-major
+// array of `outer` rows of `inner` elements (bf16, or fp32 if `f32`), rows
+// `row_bytes` apart; box = box_inner x box_outer elements, 128-byte swizzle
+// if `swizzle128`; out-of-range elements read as zero.
+bool encode_map_2d(void* map, bool f32, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 int classify_tile(int q_stream, int64_t qt, int k_stream, int64_t kt, int64_t L, int64_t M,
                   int64_t T);
 

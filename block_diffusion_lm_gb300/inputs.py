@@ -143,3 +143,49 @@ def to_f64(t):
     if t is None:
         return None
     return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+# ------------------------------------------------------------ vocabulary loss
+@dataclasses.dataclass(frozen=True)
+class CeWorkload:
+    """LM-head cross-entropy: N loss rows of hidden size Dm against a V-row head."""
+    name: str
+    N: int
+    Dm: int
+    V: int
+    chunk: int = 0            # rows per chunk (0: library default)
+    head_grad: bool = True    # False: frozen head (no dW)
+    ignore_frac: float = 0.0  # share of rows with target -1
+    seed: int = 2000
+
+    def flops(self) -> float:
+        """Logits, dH and (trained head) dW: 2 N V Dm each."""
+        return 2.0 * self.N * self.V * self.Dm * (3 if self.head_grad else 2)
+
+
+CE_WORKLOADS = {
+    "ce_tiny": CeWorkload("ce_tiny", 300, 192, 1600, chunk=128, ignore_frac=0.2, seed=2001),
+    # LM head of the dense 14B-like layer: one 16K-token sequence, 128K vocabulary
+    "lmhead14b": CeWorkload("lmhead14b", 16384, 5120, 131072, chunk=8192, seed=2002),
+    # the drafter's frozen head (no dW)
+    "lmhead_frozen": CeWorkload("lmhead_frozen", 16384, 5120, 131072, chunk=8192,
+                                head_grad=False, seed=2003),
+}
+
+
+def make_ce_inputs(w: CeWorkload, device="cuda", seed: int | None = None) -> dict:
+    """h ~ N(0, 1) [N, Dm] and W ~ N(0, 1) * 2/sqrt(Dm) [V, Dm] (logits of
+    standard deviation about 2), both rounded to bf16; targets uniform over
+    the vocabulary, a share `ignore_frac` of them set to -1.  Drawn from one
+    torch generator in the order h, W, targets, ignore mask."""
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed if seed is None else seed)
+    h = torch.randn((w.N, w.Dm), generator=g, device=device, dtype=torch.float32)
+    W = torch.randn((w.V, w.Dm), generator=g, device=device, dtype=torch.float32)
+    W = W * (2.0 / math.sqrt(w.Dm))
+    t = torch.randint(0, w.V, (w.N,), generator=g, device=device, dtype=torch.int64)
+    drop = torch.rand((w.N,), generator=g, device=device) < w.ignore_frac
+    t = torch.where(drop, torch.full_like(t, -1), t).to(torch.int32)
+    n_valid = int((t >= 0).sum().item())
+    return {"h": h.to(torch.bfloat16), "w": W.to(torch.bfloat16), "target": t,
+            "grad_scale": 1.0 / max(1, n_valid)}
