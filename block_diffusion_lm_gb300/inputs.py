@@ -170,6 +170,9 @@ CE_WORKLOADS = {
     # the drafter's frozen head (no dW)
     "lmhead_frozen": CeWorkload("lmhead_frozen", 16384, 5120, 131072, chunk=8192,
                                 head_grad=False, seed=2003),
+    # the same head on 2K rows: a case small enough for profiler captures
+    # (logits chunk 256 MiB, still twice the L2)
+    "lmhead_2k": CeWorkload("lmhead_2k", 2048, 5120, 32768, chunk=2048, seed=2004),
 }
 
 
