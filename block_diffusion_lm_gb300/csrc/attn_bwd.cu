@@ -18,7 +18,8 @@
 //   warp 2 lane 0  TMA producer: dO (2 stages)
 //   warp 1 lane 0  MMA issuer, per step i:
 //                    dV += P_i^T dO_i        (P^T read from TMEM)
-//                    dK += dS_i^T Q_i; dQ_i^T = K^T dS_i^T   (dS^T from smem)
+//                    dQ_i^T = K^T dS_i^T; dK += dS_i^T Q_i   (dS^T from smem;
+//                    dQ^T first: the compute warps wait on it, not on dK)
 //                    S^T_{i+1} = K Q_{i+1}^T; dP^T_{i+1} = V dO_{i+1}^T
 //   warps 4..7 / 8..11  compute halves 0 / 1 (query columns 64h..64h+63):
 //                  thread t owns key row t (TMEM lane t).  It turns S^T into
@@ -65,6 +66,7 @@ enum BwdBar {
   C_X_FREE = C_STAGE_FULL + 2,      // [2] per half: dS^T box read by its reduce-add
   C_SQ_FREE = C_X_FREE + 2,         // [2] per half: staging buffer read by its reduce-add
   C_ACC_DONE = C_SQ_FREE + 2,
+  C_DK_DONE,                        // dK_i complete: the dS^T boxes are free
   C_DRAIN,
   C_COUNT
 };
@@ -351,21 +353,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma_commit(&bars[C_PV_DONE]);
       umma_commit(&bars[C_DO_EMPTY + i % Lay::kDOStages]);
-      // ---- dK += dS^T Q; dQ^T = K^T dS^T
+      // ---- dQ^T = K^T dS^T first (the compute warps wait on it), then
+      //      dK += dS^T Q
       if (!mbar_wait(&bars[C_DS_READY], i & 1, p.status, abort_flag)) break;
       tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        umma_bf16_ss(tmem + Lay::kColDP, sdesc_step(k_mn, kk * 2048), sdesc_step(x_mn, kk * 2048),
+                     idesc_q, kk > 0 ? 1u : 0u);
+      umma_commit(&bars[C_DQ_FULL]);
       {
         const uint64_t b = sdesc_sw128(q_s, Lay::kBox, 1024);  // Q as MN-major B
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_bf16_ss(tmem + Lay::kColDK, sdesc_step(x_kmaj, (kk >> 2) * Lay::kXBox + (kk & 3) * 32),
                        sdesc_step(b, kk * 2048), idesc_kd, kk > 0 ? 1u : acc0);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_ss(tmem + Lay::kColDP, sdesc_step(k_mn, kk * 2048), sdesc_step(x_mn, kk * 2048),
-                       idesc_q, kk > 0 ? 1u : 0u);
       }
-      umma_commit(&bars[C_DQ_FULL]);
+      umma_commit(&bars[C_DK_DONE]);
       umma_commit(&bars[C_Q_EMPTY + st]);
       if (i + 1 < n_steps) {
         // ---- S^T_{i+1}: its columns held P^T_i, consumed once dV_i is done
@@ -496,13 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C_DQ_FREE]);
-      // stage the half's 64 dQ rows: the first kRowsX in its dS^T box, which
-      // the completed dK / dQ^T MMAs no longer read, the rest in its own
-      // buffer once the previous step's reduce-add from there has read it
-      if (r < D) {
-#pragma unroll
-        for (int c = 0; c < Lay::kRowsX; ++c) stage_x[c * D + r] = dq[c];
-      }
+      // stage the half's 64 dQ rows: the last kRowsSQ in its own buffer once
+      // the previous step's reduce-add from there has read it, the first
+      // kRowsX in its dS^T box once dK_i (the box's last reader) is done
       if (Lay::kRowsSQ > 0) {
         if (i > 0 && leader && lane == 0) {
           bulk_wait_group_read<0>();
@@ -516,6 +516,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < Lay::kRowsSQ; ++c) stage_sq[c * D + r] = dq[Lay::kRowsX + c];
         }
+      }
+      if (!mbar_wait_warp(&bars[C_DK_DONE], i & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (r < D) {
+#pragma unroll
+        for (int c = 0; c < Lay::kRowsX; ++c) stage_x[c * D + r] = dq[c];
       }
       fence_proxy_async_smem();
       __syncwarp();
