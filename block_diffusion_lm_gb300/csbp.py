@@ -35,7 +35,8 @@ class Problem(ctypes.Structure):
                 ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32),
                 ("P", ctypes.c_int32), ("tile_q", ctypes.c_int32), ("tile_kv", ctypes.c_int32),
                 ("has_clean_queries", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("window", ctypes.c_int32), ("clean_causal", ctypes.c_int32)]
+                ("window", ctypes.c_int32), ("clean_causal", ctypes.c_int32),
+                ("bwd_chunk", ctypes.c_int32)]
 
 
 class Inputs(ctypes.Structure):
@@ -114,10 +115,10 @@ def _check(fn, status):
 
 
 def make_problem(batch, L, M, Hq, Hkv, d, P=1, has_clean_queries=True, scale=None,
-                 tile=128, window=0, clean_causal=False) -> Problem:
+                 tile=128, window=0, clean_causal=False, bwd_chunk=0) -> Problem:
     return Problem(batch, L, M, Hq, Hkv, d, P, tile, tile, 1 if has_clean_queries else 0,
                    float(scale if scale is not None else d ** -0.5), int(window),
-                   1 if clean_causal else 0)
+                   1 if clean_causal else 0, int(bwd_chunk))
 
 
 def block_schedule(problem: Problem):
@@ -245,10 +246,11 @@ class BlockDiffusionAttention:
     """
 
     def __init__(self, batch, L, M, Hq, Hkv, d, P=1, has_clean_queries=True, scale=None,
-                 device="cuda", window=0, clean_causal=False):
+                 device="cuda", window=0, clean_causal=False, bwd_chunk=0):
         import torch
         self.problem = make_problem(batch, L, M, Hq, Hkv, d, P, has_clean_queries, scale,
-                                    window=window, clean_causal=clean_causal)
+                                    window=window, clean_causal=clean_causal,
+                                    bwd_chunk=bwd_chunk)
         bo, co, words, info = block_schedule(self.problem)
         self.block_owner, self.chunk_owner, self.info = bo, co, info
         self.work_host = words

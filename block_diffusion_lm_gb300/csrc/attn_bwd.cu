@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* segs = p.segs + static_cast<int64_t>(tw[3]) * kSegWords;
   const int n_segs = tw[4];
   const int n_steps = tw[5] * p.G;
+  const bool accumulate = (tw[6] & 1) != 0;  // dK/dV into the fp32 accumulators
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C_COUNT; ++i) {
@@ -557,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(k_stream ? p.dk[1] : p.dk[0]) +
                           ((static_cast<int64_t>(bz) * p.L + kpos) * p.Hkv + kvh) * D;
       if (n_steps == 0) {
-        if (k_valid) {
+        if (k_valid && !accumulate) {
           for (int c = 0; c < D; c += 8) {
             *reinterpret_cast<uint4*>(dv + c) = make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4*>(dk + c) = make_uint4(0, 0, 0, 0);
@@ -565,16 +566,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (ok && mbar_wait_warp(&bars[C_ACC_DONE], 0, p.status, abort_flag)) {
         tc_fence_after_sync();
+        // windowed tasks add their share into the fp32 accumulators
+        const int64_t acc_row =
+            ((static_cast<int64_t>(k_stream) * p.batch + bz) * p.L + kpos) * p.Hkv + kvh;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           __nv_bfloat16* dstp = half ? dk : dv;
           const uint32_t col = half ? Lay::kColDK : Lay::kColDV;
           const float mul = half ? p.scale : 1.f;
+          float* accp = (half ? p.dk_acc : p.dv_acc);
 #pragma unroll 1
           for (int ch = 0; ch < D / 32; ++ch) {
             float v[32];
             tmem_ld32(tmem + lane_base + col + ch * 32, v);
-            if (k_valid) {
+            if (k_valid && accumulate) {
+              float4* a4 = reinterpret_cast<float4*>(accp + acc_row * D + ch * 32);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                atomicAdd(a4 + e, make_float4(v[4 * e] * mul, v[4 * e + 1] * mul, v[4 * e + 2] * mul,
+                                              v[4 * e + 3] * mul));
+            } else if (k_valid) {
 #pragma unroll
               for (int e = 0; e < 32; e += 8) {
                 uint4 u;

@@ -103,7 +103,8 @@ bool make_map_dqacc(CUtensorMap* m, void* base, int64_t Hq, int d, int64_t L, in
 }
 
 struct WsLayout {
-  size_t status = 0, part_o = 0, part_lse = 0, dsum = 0, dq_acc = 0, total = 0;
+  size_t status = 0, part_o = 0, part_lse = 0, dsum = 0, dq_acc = 0, dk_acc = 0, dv_acc = 0,
+         total = 0;
 };
 
 WsLayout ws_layout(const csbp_problem* p, int which) {
@@ -122,6 +123,12 @@ WsLayout ws_layout(const csbp_problem* p, int which) {
     off += round256(2 * rows * p->Hq * 4);
     w.dq_acc = off;
     off += round256(2 * rows * p->Hq * p->d * 4);
+    if (bwd_windowed(p)) {
+      w.dk_acc = off;
+      off += round256(2 * rows * p->Hkv * p->d * 4);
+      w.dv_acc = off;
+      off += round256(2 * rows * p->Hkv * p->d * 4);
+    }
   }
   w.total = off;
   return w;
@@ -457,11 +464,33 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
   bp.dv[0] = dv_clean;
   bp.dv[1] = dv_corr;
   bp.status = reinterpret_cast<int*>(ws + wl.status);
+  bp.dk_acc = nullptr;
+  bp.dv_acc = nullptr;
+  const bool windowed = bwd_windowed(problem);
+  const int64_t kv_elems = rows * p.Hkv * p.d;  // per key stream
+  if (windowed) {
+    bp.dk_acc = reinterpret_cast<float*>(ws + wl.dk_acc);
+    bp.dv_acc = reinterpret_cast<float*>(ws + wl.dv_acc);
+    if (launch_fill(bp.dk_acc, 2 * kv_elems, 0.f, stream) != cudaSuccess ||
+        launch_fill(bp.dv_acc, 2 * kv_elems, 0.f, stream) != cudaSuccess)
+      return CSBP_ERR_CUDA;
+  }
   const int timed = timer_begin(1, stream);
   const cudaError_t be = launch_bwd(p.d, maps, bp, info->n_bwd_tasks, stream);
   timer_end(timed, stream);
   if (be != cudaSuccess) return CSBP_ERR_CUDA;
 
+  if (windowed) {
+    void* dk_s[2] = {dk_clean, dk_corr};
+    void* dv_s[2] = {dv_clean, dv_corr};
+    for (int ks = 0; ks < 2; ++ks) {
+      if (launch_dq_convert(bp.dk_acc + ks * kv_elems, dk_s[ks], kv_elems, 1.f, stream) !=
+              cudaSuccess ||
+          launch_dq_convert(bp.dv_acc + ks * kv_elems, dv_s[ks], kv_elems, 1.f, stream) !=
+              cudaSuccess)
+        return CSBP_ERR_CUDA;
+    }
+  }
   void* dq_s[2] = {dq_clean, dq_corr};
   for (int qs = hc ? 0 : 1; qs < 2; ++qs) {
     if (launch_dq_convert(dq_acc + qs * stream_elems, dq_s[qs], stream_elems, p.scale, stream) !=

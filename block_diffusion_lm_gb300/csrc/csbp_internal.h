@@ -24,6 +24,18 @@ enum HeaderWord {
 
 csbp_status validate_problem(const csbp_problem* p);
 
+// Backward query-tile window (csbp_problem::bwd_chunk, 0 = default) and
+// whether the problem's backward runs in windows with fp32 dK/dV
+// accumulation: with an explicit window, once a key tile can be read by more
+// query tiles than that; by default (windows of 512) only past 2048 query
+// tiles, where long walks let the CTAs of a wave drift apart (measured: a
+// 1M-token corrupted-only problem gains 3.5 %, a 128K two-copy one loses 5 %
+// with windows).
+constexpr int32_t kDefaultBwdChunk = 512;
+constexpr int32_t kDefaultBwdWindowFrom = 2048;
+int64_t bwd_chunk_tiles(const csbp_problem* p);
+bool bwd_windowed(const csbp_problem* p);
+
 // Kernel timing (csbp_kernel_timing): kinds 0 fwd, 1 bwd, 2 CE logits GEMM,
 // 3 CE row kernel, 4 CE dH GEMM, 5 CE dW GEMM.  timer_begin returns the pair
 // index to close with timer_end, or -1 when not recording.
@@ -73,6 +85,8 @@ struct BwdParams {
   float* dq_acc;         // [2][batch][L][Hq][d] fp32, pre-zeroed
   void* dk[2];           // bf16 [batch][L][Hkv][d] per key stream
   void* dv[2];
+  float* dk_acc;         // windowed backward: fp32 [2][batch][L][Hkv][d], pre-zeroed
+  float* dv_acc;
   int* status;
 };
 

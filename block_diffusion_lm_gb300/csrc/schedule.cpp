@@ -96,6 +96,8 @@ struct Task {
   std::vector<Seg> segs;
   int32_t cost;
   int64_t canon;
+  int32_t flags = 0;   // bwd: bit0 = dK/dV into the fp32 accumulators
+  int32_t window = 0;  // bwd: query-tile window, 0 = the last one
 };
 
 // Append tile `t` with class `cls` (1/2) of `stream` to a run-length list of
@@ -126,6 +128,7 @@ csbp_status validate_problem(const csbp_problem* p) {
   if (p->tile_q < 1 || p->tile_kv < 1) return CSBP_ERR_INVALID;
   if (p->has_clean_queries != 0 && p->has_clean_queries != 1) return CSBP_ERR_INVALID;
   if (p->window < 0 || (p->clean_causal != 0 && p->clean_causal != 1)) return CSBP_ERR_INVALID;
+  if (p->bwd_chunk < 0) return CSBP_ERR_INVALID;
   if (p->d != 64 && p->d != 128) return CSBP_ERR_UNSUPPORTED;
   if (p->tile_q != p->tile_kv) return CSBP_ERR_UNSUPPORTED;
   if (p->P > 1) {
@@ -135,6 +138,15 @@ csbp_status validate_problem(const csbp_problem* p) {
     if (p->P + 1 > kMaxParts) return CSBP_ERR_UNSUPPORTED;
   }
   return CSBP_OK;
+}
+
+int64_t bwd_chunk_tiles(const csbp_problem* p) {
+  return p->bwd_chunk > 0 ? p->bwd_chunk : kDefaultBwdChunk;
+}
+
+bool bwd_windowed(const csbp_problem* p) {
+  const int64_t nT = (static_cast<int64_t>(p->L) + p->tile_q - 1) / p->tile_q;
+  return nT > (p->bwd_chunk > 0 ? p->bwd_chunk : kDefaultBwdWindowFrom);
 }
 
 }  // namespace csbp
@@ -223,7 +235,10 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
   }
   (void)n_qs;
 
-  // ---- backward tasks: per key tile, segments over query tiles
+  // ---- backward tasks: per key tile, segments over query tiles (per key
+  //      tile and query-tile window when the ranges are long)
+  const bool windowed = bwd_windowed(problem);
+  const int64_t chunk = bwd_chunk_tiles(problem);
   std::vector<Task> bwd;
   for (int ks = 0; ks < 2; ++ks) {
     for (int64_t kt = 0; kt < nT; ++kt) {
@@ -240,11 +255,33 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
       }
       // emitted even when no query reads the tile: its dK/dV are then zero
       t.canon = (int64_t)ks * nT + kt;
-      bwd.push_back(std::move(t));
+      if (!windowed || t.segs.empty()) {
+        t.flags = windowed ? 1 : 0;
+        bwd.push_back(std::move(t));
+        continue;
+      }
+      // one task per window of `chunk` query tiles, counted from the last
+      // tile, so the CTAs of a wave walk the same window in step and share
+      // its Q / dO tiles and dQ rows in L2 however long the whole range is
+      for (int32_t j = 0;; ++j) {
+        const int64_t hi = nT - (int64_t)j * chunk;
+        if (hi <= 0) break;
+        const int64_t lo = hi - chunk > 0 ? hi - chunk : 0;
+        Task u{t.a_stream, t.a_tile, t.part, {}, 0, t.canon, 1, j};
+        for (const Seg& g : t.segs) {
+          const int64_t b = g.begin > lo ? g.begin : lo;
+          const int64_t e = g.end < hi ? g.end : hi;
+          if (b >= e) continue;
+          u.segs.push_back({g.stream, (int32_t)b, (int32_t)e, g.flags});
+          u.cost += (int32_t)(e - b);
+        }
+        if (!u.segs.empty()) bwd.push_back(std::move(u));
+      }
     }
   }
 
   auto heavy_first = [](const Task& a, const Task& b) {
+    if (a.window != b.window) return a.window < b.window;
     if (a.cost != b.cost) return a.cost > b.cost;
     return a.canon < b.canon;
   };
@@ -299,6 +336,8 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
       tw[3] = (int32_t)s;
       tw[4] = (int32_t)t.segs.size();
       tw[5] = t.cost;
+      tw[6] = t.flags;
+      tw[7] = t.window;
       for (const Seg& g : t.segs) {
         int32_t* sw = w + off_s + s * kSegWords;
         sw[0] = g.stream;

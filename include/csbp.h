@@ -84,6 +84,16 @@ typedef struct {
                            layers, [Blog] "实验数字：256K 上下文下的主结果")      */
   int32_t clean_causal; /* 0: clean queries block-causal over the clean copy;
                            1: token-causal (key j <= query i)             */
+  int32_t bwd_chunk;    /* backward query-tile window, >= 0.  When a key
+                           tile can be read by more query tiles than this,
+                           every backward task covers one window of query
+                           tiles counted from the last tile, the CTAs of a
+                           wave walk the same window, and dK/dV gather in
+                           fp32 workspace accumulators (then bf16).  0: the
+                           library default, windows of 512 once the sequence
+                           has more than 2048 query tiles.  A schedule
+                           setting: results differ only by fp32 summation
+                           order.                                         */
 } csbp_problem;
 
 /* Device input tensors, bf16 [batch][L][H][d] contiguous (H = Hq for q,
@@ -114,8 +124,12 @@ typedef struct {
  *   fwd segment (4 words): kv_stream, kv_tile_begin, kv_tile_end (exclusive),
  *                 flags (bit0 = partial: tiles need the in-tile mask)
  *   bwd task (8 words): kv_stream, kv_tile, part, seg_begin, seg_count,
- *                 q_tiles, 0, 0  (one per key tile of both copies, including
- *                 tiles no query reads, whose dK/dV are zero)
+ *                 q_tiles, flags (bit0 = dK/dV add into the fp32
+ *                 accumulators), window (0 = the last bwd_chunk query
+ *                 tiles, 1 = the ones before, ...).  One task per key tile
+ *                 of both copies, including tiles no query reads (dK/dV
+ *                 zero); with windows, one per key tile and window that
+ *                 holds a query tile reading it.
  *   bwd segment (4 words): q_stream, q_tile_begin, q_tile_end, flags
  * Streams: 0 = clean copy, 1 = corrupted copy.  Part of a key tile: the
  * owner shard of its clean chunk (clean keys) or P (corrupted keys).

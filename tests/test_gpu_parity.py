@@ -33,13 +33,14 @@ def rel_fro(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
-def run_gpu(w: Workload, L=None, seed=None, P=None):
+def run_gpu(w: Workload, L=None, seed=None, P=None, bwd_chunk=0):
     L = w.L if L is None else L
     t = make_inputs(w, "cuda", seed=seed, L=L)
     attn = csbp.BlockDiffusionAttention(w.batch, L, w.M, w.Hq, w.Hkv, w.d,
                                         P=w.P if P is None else P,
                                         has_clean_queries=w.has_clean_queries,
-                                        window=w.window, clean_causal=w.clean_causal)
+                                        window=w.window, clean_causal=w.clean_causal,
+                                        bwd_chunk=bwd_chunk)
     out = attn.forward(t)
     g = attn.backward(t, out)
     attn.check()
@@ -78,7 +79,28 @@ SMALL = [
 
 @pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
 def test_small_cases_match_oracle_elementwise(w):
-    t, (oc, ox, lse), g = run_gpu(w)
+    _check_against_oracle(w)
+
+
+# the backward in query-tile windows (fp32 dK/dV accumulation), forced on
+# small problems by a window of a few query tiles
+WINDOWED = [
+    (WORKLOADS["tiny"], 3),
+    (Workload("gqa_ragged_w", 1, 400, 16, 4, 2, 128, seed=40), 1),
+    (Workload("drafter_small_w", 1, 512, 16, 4, 1, 128, has_clean_queries=False, seed=41), 2),
+    (Workload("win_causal_w", 1, 640, 16, 4, 2, 64, window=150, clean_causal=True, seed=42), 2),
+    (Workload("sharded_w", 1, 1024, 16, 4, 2, 128, P=2, seed=43), 3),
+    (Workload("batch2_w", 2, 384, 32, 2, 1, 128, seed=44), 1),
+]
+
+
+@pytest.mark.parametrize("w,chunk", WINDOWED, ids=[f"{w.name}-c{c}" for w, c in WINDOWED])
+def test_windowed_backward_matches_oracle_elementwise(w, chunk):
+    _check_against_oracle(w, bwd_chunk=chunk)
+
+
+def _check_against_oracle(w, bwd_chunk=0):
+    t, (oc, ox, lse), g = run_gpu(w, bwd_chunk=bwd_chunk)
     for b in range(w.batch):
         f = {k: (to_f64(v[b]) if v is not None else None) for k, v in t.items()}
         Oc, Ox, Z = O.bd_attention_fwd(f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"],

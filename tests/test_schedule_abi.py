@@ -150,7 +150,12 @@ def test_drafter_schedule_count():
     assert st == -6  # capacity query
     nT = w.L // 128
     assert info.tile_pairs == nT * (nT + 1) // 2 + nT
-    assert info.n_bwd_tasks == 2 * nT
+    # windows of 512 query tiles: clean key tile kt is read by query tiles
+    # kt .. nT-1, i.e. by ceil((nT - kt) / 512) windows; corrupted key tiles
+    # by their own query tile only
+    c = 512
+    assert info.n_bwd_tasks == sum(-(-m // c) for m in range(1, nT + 1)) + nT
+    assert info.n_bwd_tasks == c * (nT // c) * (nT // c + 1) // 2 + nT
 
 
 def test_windowed_full_size_schedule_count():
@@ -215,3 +220,54 @@ def test_entry_points_reject_bad_arguments_without_launching():
     inp = csbp.Inputs(bad, bad, bad, bad, bad, bad)
     assert L.csbp_attn_fwd(ctypes.byref(prob), ctypes.byref(inp), bad, ctypes.byref(info),
                            bad, bad, bad, bad, 1 << 20, None) == -1
+
+
+@pytest.mark.parametrize("L,M,T,clean,W,causal,chunk", [
+    (1024, 16, 128, True, 0, False, 2), (1024, 32, 128, False, 0, False, 3),
+    (1152, 64, 128, True, 300, True, 1), (512, 16, 32, True, 0, False, 5),
+    (1040, 16, 128, True, 0, True, 4),
+])
+def test_windowed_backward_tasks_partition_the_tile_set(L, M, T, clean, W, causal, chunk):
+    """With a query-tile window smaller than the tile count, every backward
+    task covers one window (counted from the last query tile), flags its
+    dK/dV for fp32 accumulation, and the tasks together hold every allowed
+    (query tile, key tile) pair exactly once; windows run in order, heaviest
+    first within a window."""
+    prob = csbp.make_problem(1, L, M, 2, 1, 64, has_clean_queries=clean, tile=T, window=W,
+                             clean_causal=causal, bwd_chunk=chunk)
+    _, _, words, info = csbp.block_schedule(prob)
+    h = words[:16]
+    off_bt, off_bs = int(h[13]), int(h[14])
+    nT = -(-L // T)
+    want = {x[:4] for x in O.tile_pairs(L, M, T, T, 1, clean, W, causal)}
+    seen = []
+    order = []
+    for t in range(info.n_bwd_tasks):
+        ks, kt, part, sb, sc, cost, flags, win = (int(x) for x in
+                                                  words[off_bt + 8 * t: off_bt + 8 * t + 8])
+        assert flags == 1
+        lo, hi = max(0, nT - (win + 1) * chunk), nT - win * chunk
+        n = 0
+        for s in range(sb, sb + sc):
+            qs, b, e, fl = (int(x) for x in words[off_bs + 4 * s: off_bs + 4 * s + 4])
+            assert lo <= b < e <= hi
+            for qt in range(b, e):
+                seen.append((qs, qt, ks, kt))
+                n += 1
+        assert n == cost
+        order.append((win, -cost))
+    assert len(seen) == len(set(seen))
+    assert set(seen) == want
+    assert order == sorted(order)
+
+
+def test_backward_is_not_windowed_below_the_window():
+    """Up to `bwd_chunk` query tiles per key tile the list keeps one task per
+    key tile, with bf16 dK/dV written directly (flags 0)."""
+    prob = csbp.make_problem(1, 1024, 16, 2, 1, 64, bwd_chunk=8)
+    _, _, words, info = csbp.block_schedule(prob)
+    off_bt = int(words[13])
+    assert info.n_bwd_tasks == 2 * 8
+    assert all(int(words[off_bt + 8 * t + 6]) == 0 for t in range(info.n_bwd_tasks))
+    prob.bwd_chunk = -1
+    assert csbp.workspace_bytes(prob, 1) == 0
