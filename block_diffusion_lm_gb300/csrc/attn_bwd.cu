@@ -203,9 +203,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // CTA order.  kv_major: (batch, KV head) outer, task inner, so the CTAs
+  // resident together hold key tiles of one KV head, walk the same query
+  // tiles of the same few query heads and share those Q / dO tiles and dQ
+  // rows in L2 (long sequences: many waves of similar-length tasks per KV
+  // head).  Otherwise task outer: the heaviest tasks of every KV head run
+  // together, so a wave holds tasks of similar length (short sequences).
   const int hb = p.Hkv * p.batch;
-  const int task = blockIdx.x / hb;
-  const int rem = blockIdx.x - task * hb;
+  const int n_tasks = static_cast<int>(gridDim.x) / hb;
+  int task, rem;
+  if (p.kv_major) {
+    task = static_cast<int>(blockIdx.x) % n_tasks;
+    rem = static_cast<int>(blockIdx.x) / n_tasks;
+  } else {
+    task = static_cast<int>(blockIdx.x) / hb;
+    rem = static_cast<int>(blockIdx.x) - task * hb;
+  }
   const int bz = rem / p.Hkv;
   const int kvh = rem - bz * p.Hkv;
   const int32_t* tw = p.tasks + static_cast<int64_t>(task) * kTaskWords;

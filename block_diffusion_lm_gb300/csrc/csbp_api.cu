@@ -475,6 +475,16 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
         launch_fill(bp.dv_acc, 2 * kv_elems, 0.f, stream) != cudaSuccess)
       return CSBP_ERR_CUDA;
   }
+  // KV-head-major CTA order once each KV head has at least four waves of
+  // tasks (measured: +33 % on a 128K corrupted-only backward, -8 % on a 16K
+  // two-copy one, where a KV head's tasks span less than two waves)
+  {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return CSBP_ERR_CUDA;
+    bp.kv_major = (static_cast<int64_t>(info->n_bwd_tasks) >= 4 * static_cast<int64_t>(sms)) ? 1 : 0;
+  }
   const int timed = timer_begin(1, stream);
   const cudaError_t be = launch_bwd(p.d, maps, bp, info->n_bwd_tasks, stream);
   timer_end(timed, stream);

@@ -87,6 +87,7 @@ struct BwdParams {
   void* dv[2];
   float* dk_acc;         // windowed backward: fp32 [2][batch][L][Hkv][d], pre-zeroed
   float* dv_acc;
+  int32_t kv_major;      // CTA order: 1 = (batch, KV head) outer, task inner
   int* status;
 };
 
