@@ -58,26 +58,50 @@ BWD_KERNEL_SOURCES = ("attn_bwd.cu", "ptx_sm100.cuh", "csbp_internal.h")
 
 
 def bwd_kernel_source_hash():
+    return source_hash(BWD_KERNEL_SOURCES)
+
+
+CE_KERNEL_SOURCES = ("vocab_ce.cu", "ptx_sm100.cuh", "csbp_internal.h")
+
+
+def source_hash(names):
     h = hashlib.sha256()
-    for name in BWD_KERNEL_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "block_diffusion_lm_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
+
+
+def profile_fields(path):
+    """`- key: value` lines of a committed ncu summary."""
+    fields = {}
+    if os.path.exists(path):
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip().strip("`- ")] = v.strip().strip("`")
+    return fields
+
+
+def recorded_ce_traffic(workload, kernel):
+    """DRAM bytes per launch of one CE GEMM (`logits_gemm`, `dh_gemm`,
+    `dw_gemm`) from the committed ncu summary, or None if there is none or
+    the kernel changed since it was taken."""
+    fields = profile_fields(os.path.join(ROOT, "profiles", f"ce_gemm_{workload}_dram.md"))
+    if fields.get("kernel_source_sha256") != source_hash(CE_KERNEL_SOURCES):
+        return None
+    try:
+        return int(fields[f"{kernel}_dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def recorded_traffic(workload):
     """DRAM bytes (read + write) per bwd_kernel launch from the committed ncu
     summary of this workload, or None if there is none or the kernel changed
     since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"bwd_kernel_{workload}_dram.md")
-    if not os.path.exists(path):
-        return None
-    fields = {}
-    with open(path) as f:
-        for line in f:
-            if ":" in line:
-                k, v = line.split(":", 1)
-                fields[k.strip().strip("`- ")] = v.strip().strip("`")
+    fields = profile_fields(os.path.join(ROOT, "profiles", f"bwd_kernel_{workload}_dram.md"))
     if fields.get("kernel_source_sha256") != bwd_kernel_source_hash():
         return None
     try:
@@ -393,7 +417,8 @@ def bench_ce(args, w, rank, world, local):
                      "frac": achieved / peak,
                      "peak_source": f"bf16_tflops_sustained of {pk['source']}",
                      "launch_ms": kernels[top]["avg_launch_ms"],
-                     "launches_timed": kernels[top]["launches"], "traffic": None},
+                     "launches_timed": kernels[top]["launches"],
+                     "traffic": recorded_ce_traffic(w.name, top)},
         "e2e": e2e,
         "gpu_launches": n_chunks * (4 if w.head_grad else 3) * args.steps,
         "clocks": clocks,
