@@ -61,7 +61,8 @@ def bwd_kernel_source_hash():
     return source_hash(BWD_KERNEL_SOURCES)
 
 
-CE_KERNEL_SOURCES = ("vocab_ce.cu", "ptx_sm100.cuh", "csbp_internal.h")
+# the CE kernels' device code comes from these two files alone
+CE_KERNEL_SOURCES = ("vocab_ce.cu", "ptx_sm100.cuh")
 
 
 def source_hash(names):
@@ -247,12 +248,42 @@ def cpu_oracle_sample(w, seconds, seed=7):
             "extrapolated_step_s": full / (value * 1e12)}
 
 
+# ----------------------------------------------------------- HBM kernels
+def hbm_kernels(w, csbp):
+    """GB/s of the HBM-bound launches of the timed steps: algorithmic bytes
+    per launch (each input read once, each output written once) over the
+    average CUDA-event duration of that launch, against the measured copy
+    bandwidth."""
+    d, rows = w.d, w.batch * w.L
+    per_launch = {
+        # n partial (O fp32, z fp32) read, O bf16 + z written, per (row, head)
+        6: ("lse_merge", w.L * w.Hq * ((w.P + 1) * (4 * d + 4) + 2 * d + 4)),
+        # O, dO read; D and the zeroed fp32 dQ row written
+        7: ("bwd_pre", rows * w.Hq * (8 * d + 4)),
+        # fp32 dQ read, bf16 dQ written
+        8: ("dq_convert", rows * w.Hq * 6 * d),
+        # fp32 dK and dV read, bf16 written (windowed backward)
+        9: ("dkv_convert", 2 * rows * w.Hkv * 6 * d),
+    }
+    peak = peaks()["hbm"]
+    out = {}
+    for kind, (name, nbytes) in per_launch.items():
+        ms, n = csbp.kernel_timing_read_kind(kind)
+        if n:
+            gbs = nbytes / (ms / n * 1e-3) / 1e9
+            out[name] = {"launches": n, "avg_launch_ms": ms / n, "bytes_per_launch": nbytes,
+                         "gbs": gbs, "frac_of_measured_hbm": gbs / peak}
+    return out or None
+
+
 # --------------------------------------------------------------- launches
 def launches_per_step(w):
     """Kernels this library launches per fwd+bwd step (mirrors csbp_api.cu)."""
     n_qs = 2 if w.has_clean_queries else 1
     fwd = 1 + ((1 + n_qs * w.batch) if w.P > 1 else 0)   # [fill] + fwd + [merges]
     bwd = n_qs + 1 + n_qs                                  # pre per stream + main + convert
+    if -(-w.L // 128) > 2048:                              # backward in query-tile windows:
+        bwd += 2 + 4                                       # zero dK/dV acc, convert per stream
     return fwd + bwd
 
 
@@ -529,6 +560,7 @@ def main():
     clocks = sampler.stop()
     csbp.kernel_timing(False)
     fwd_k_ms, n_fwd_k, bwd_k_ms, n_bwd_k = csbp.kernel_timing_read()
+    hbm = hbm_kernels(w, csbp)
     attn.check(stream)
     total_ms = start_all.elapsed_time(end_all)
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
@@ -572,6 +604,7 @@ def main():
                      "peak_source": f"bf16_tflops_sustained of {pk['source']}",
                      "launch_ms": bwd_kernel_ms, "launches_timed": n_bwd_k,
                      "traffic": recorded_traffic(w.name)},
+        "hbm_kernels": hbm,
         "e2e": e2e,
         "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clocks,

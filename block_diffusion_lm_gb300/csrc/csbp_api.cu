@@ -376,7 +376,10 @@ extern "C" csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inp
         }
         void* oo = static_cast<uint16_t*>(qs ? o_corr : o_clean) + bz * slab_o;  // bf16 elements
         float* zo = lse + (static_cast<int64_t>(bz) * 2 + qs) * slab_z;
-        if (launch_lse_merge(a, n_parts, p.L, p.Hq, p.d, oo, zo, stream) != cudaSuccess)
+        const int tm = timer_begin(6, stream);
+        const cudaError_t me = launch_lse_merge(a, n_parts, p.L, p.Hq, p.d, oo, zo, stream);
+        timer_end(tm, stream);
+        if (me != cudaSuccess)
           return CSBP_ERR_CUDA;
       }
     }
@@ -437,8 +440,11 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
   const void* o_s[2] = {o_clean, o_corr};
   const void* do_s[2] = {do_clean, do_corr};
   for (int qs = hc ? 0 : 1; qs < 2; ++qs) {
-    if (launch_bwd_pre(p.d, o_s[qs], do_s[qs], dsum + qs * rows * p.Hq, dq_acc + qs * stream_elems,
-                       rows, p.Hq, p.L, stream) != cudaSuccess)
+    const int tp = timer_begin(7, stream);
+    const cudaError_t pe = launch_bwd_pre(p.d, o_s[qs], do_s[qs], dsum + qs * rows * p.Hq,
+                                          dq_acc + qs * stream_elems, rows, p.Hq, p.L, stream);
+    timer_end(tp, stream);
+    if (pe != cudaSuccess)
       return CSBP_ERR_CUDA;
   }
 
@@ -456,8 +462,6 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
   bp.clean_causal = p.clean_causal;
   bp.scale_log2 = p.scale * 1.4426950408889634f;
   bp.scale = p.scale;
-  bp.lse = lse;
-  bp.Dsum = dsum;
   bp.dq_acc = dq_acc;
   bp.dk[0] = dk_clean;
   bp.dk[1] = dk_corr;
@@ -494,18 +498,22 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
     void* dk_s[2] = {dk_clean, dk_corr};
     void* dv_s[2] = {dv_clean, dv_corr};
     for (int ks = 0; ks < 2; ++ks) {
-      if (launch_dq_convert(bp.dk_acc + ks * kv_elems, dk_s[ks], kv_elems, 1.f, stream) !=
-              cudaSuccess ||
-          launch_dq_convert(bp.dv_acc + ks * kv_elems, dv_s[ks], kv_elems, 1.f, stream) !=
-              cudaSuccess)
-        return CSBP_ERR_CUDA;
+      const int tc = timer_begin(9, stream);
+      const cudaError_t ce =
+          launch_dq_convert(bp.dk_acc + ks * kv_elems, dk_s[ks], kv_elems, 1.f, stream) != cudaSuccess
+              ? cudaErrorUnknown
+              : launch_dq_convert(bp.dv_acc + ks * kv_elems, dv_s[ks], kv_elems, 1.f, stream);
+      timer_end(tc, stream);
+      if (ce != cudaSuccess) return CSBP_ERR_CUDA;
     }
   }
   void* dq_s[2] = {dq_clean, dq_corr};
   for (int qs = hc ? 0 : 1; qs < 2; ++qs) {
-    if (launch_dq_convert(dq_acc + qs * stream_elems, dq_s[qs], stream_elems, p.scale, stream) !=
-        cudaSuccess)
-      return CSBP_ERR_CUDA;
+    const int tq = timer_begin(8, stream);
+    const cudaError_t qe = launch_dq_convert(dq_acc + qs * stream_elems, dq_s[qs], stream_elems,
+                                             p.scale, stream);
+    timer_end(tq, stream);
+    if (qe != cudaSuccess) return CSBP_ERR_CUDA;
   }
   return CSBP_OK;
 }

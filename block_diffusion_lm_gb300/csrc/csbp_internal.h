@@ -37,9 +37,11 @@ int64_t bwd_chunk_tiles(const csbp_problem* p);
 bool bwd_windowed(const csbp_problem* p);
 
 // Kernel timing (csbp_kernel_timing): kinds 0 fwd, 1 bwd, 2 CE logits GEMM,
-// 3 CE row kernel, 4 CE dH GEMM, 5 CE dW GEMM.  timer_begin returns the pair
-// index to close with timer_end, or -1 when not recording.
-constexpr int kTimerKinds = 6;
+// 3 CE row kernel, 4 CE dH GEMM, 5 CE dW GEMM, 6 LSE merge, 7 backward
+// preprocess, 8 dQ convert, 9 dK/dV convert (windowed backward).
+// timer_begin returns the pair index to close with timer_end, or -1 when not
+// recording.
+constexpr int kTimerKinds = 10;
 int timer_begin(int kind, void* stream);
 void timer_end(int i, void* stream);
 
@@ -80,8 +82,6 @@ struct BwdParams {
   int32_t window, clean_causal;  // mask options (0 = none / block-causal)
   float scale_log2;
   float scale;
-  const float* lse;      // [batch][2][Hq][L]
-  const float* Dsum;     // [2][batch][Hq][L]
   float* dq_acc;         // [2][batch][L][Hq][d] fp32, pre-zeroed
   void* dk[2];           // bf16 [batch][L][Hkv][d] per key stream
   void* dv[2];

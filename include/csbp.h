@@ -237,8 +237,9 @@ csbp_status csbp_check_status(void* workspace, void* stream);
  * default.  csbp_kernel_timing(1) creates a pool of CUDA events on the
  * current device and clears the record; while it is on, every csbp_attn_fwd
  * and csbp_attn_bwd call records an event pair on its stream around its main
- * kernel (fwd_kernel / bwd_kernel), and csbp_vocab_ce one around each of its
- * launches, up to 4096 pairs in all (later launches are not timed).
+ * kernel (fwd_kernel / bwd_kernel) and its HBM-bound launches, and
+ * csbp_vocab_ce one around each of its launches, up to 4096 pairs in all
+ * (later launches are not timed).
  * csbp_kernel_timing(0) stops recording and keeps the record.
  * csbp_kernel_timing_read synchronises the recorded events and returns the
  * summed device milliseconds and launch counts of each kind (any output
@@ -247,10 +248,13 @@ csbp_status csbp_kernel_timing(int32_t enable);
 csbp_status csbp_kernel_timing_read(double* fwd_ms, int32_t* n_fwd, double* bwd_ms,
                                     int32_t* n_bwd);
 
-/* The same record by kernel kind: 0 fwd_kernel, 1 bwd_kernel, and for
+/* The same record by kernel kind: 0 fwd_kernel, 1 bwd_kernel; for
  * csbp_vocab_ce (csbp_vocab_ce.h) 2 the logits GEMM, 3 the row kernel
- * (LSE, loss, g), 4 the dH GEMM, 5 the dW GEMM, one pair per launch.
- * CSBP_ERR_INVALID for another kind. */
+ * (LSE, loss, g), 4 the dH GEMM, 5 the dW GEMM; and the HBM-bound launches
+ * of the attention calls: 6 the LSE merge (one per query stream and batch
+ * entry), 7 the backward preprocess and 8 the dQ convert (one per query
+ * stream), 9 the dK/dV converts of a windowed backward (one pair per key
+ * stream).  One event pair per launch.  CSBP_ERR_INVALID for another kind. */
 csbp_status csbp_kernel_timing_read_kind(int32_t kind, double* ms, int32_t* n);
 
 /* Human-readable name of a status code (static string). */
