@@ -103,13 +103,20 @@ struct BwdLayout {
 };
 
 // Walk over the (query tile, segment, query head in group) steps of a task:
-// query tiles from the last down, every segment (query stream) that holds the
-// tile, then the heads of the GQA group.  Every key tile of a stream is read by
-// the last query tiles, so CTAs that start together stay on the same query
-// tile, and their dQ reduce-adds and Q / dO loads of that tile meet in L2.
+// query tiles in some order, every segment (query stream) that holds the
+// tile, then the heads of the GQA group.
+//  - Default: from the last tile down.  Every key tile of a stream is read by
+//    the last query tiles, so CTAs that start together stay on the same query
+//    tile, and their dQ reduce-adds and Q / dO loads of that tile meet in L2.
+//  - Modular (sliding-window masks): the task's tiles span lo .. lo + n - 1
+//    and step tau visits the one that is congruent to -tau mod n.  Key tile k
+//    is read by query tiles k .. k + n - 1 for a fixed n, so at step tau the
+//    CTAs of a wave all visit tiles of one residue class, and a query tile's
+//    n readers take it in the same step rather than n steps apart.
 struct QWalk {
   const int32_t* seg0;
   int n_segs, G, g, si, t, stream, flags;
+  int lo, n, tau;  // modular order (n > 0)
   __device__ bool holds(int s, int tile) const {
     const int32_t* x = seg0 + s * kSegWords;
     return x[1] <= tile && tile < x[2];
@@ -124,23 +131,50 @@ struct QWalk {
     stream = x[0];
     flags = x[3];
   }
-  __device__ void start(const int32_t* s, int n, int group) {
+  __device__ int mod_tile(int k) const {  // tile of modular step k
+    const int r = ((-k - lo) % n + n) % n;
+    return lo + r;
+  }
+  __device__ void start(const int32_t* s, int n_seg, int group, bool modular) {
     seg0 = s;
-    n_segs = n;
+    n_segs = n_seg;
     G = group;
     g = 0;
     t = -1;
-    for (int k = 0; k < n; ++k) t = max(t, s[k * kSegWords + 2] - 1);
-    si = find(0);
+    lo = 0x7fffffff;
+    n = 0;
+    tau = 0;
+    for (int k = 0; k < n_seg; ++k) {
+      t = max(t, s[k * kSegWords + 2] - 1);
+      lo = min(lo, s[k * kSegWords + 1]);
+    }
+    if (modular && t >= lo) {
+      n = t - lo + 1;
+      t = mod_tile(0);
+      si = find(0);
+      while (si >= n_segs && ++tau < n) {
+        t = mod_tile(tau);
+        si = find(0);
+      }
+    } else {
+      si = find(0);
+    }
     if (si < n_segs) load_seg();
   }
   __device__ void next() {
     if (++g < G) return;
     g = 0;
     si = find(si + 1);
-    while (si >= n_segs && t > 0) {
-      --t;
-      si = find(0);
+    if (n > 0) {
+      while (si >= n_segs && ++tau < n) {
+        t = mod_tile(tau);
+        si = find(0);
+      }
+    } else {
+      while (si >= n_segs && t > 0) {
+        --t;
+        si = find(0);
+      }
     }
     if (si < n_segs) load_seg();
   }
@@ -272,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   k_tile * kTile, bz);
     }
     QWalk w;
-    w.start(segs, n_segs, p.G);
+    w.start(segs, n_segs, p.G, p.window > 0);
     int nq = 0;
     bool ok = true;
     for (int i = 0; i < n_steps && ok; ++i, w.next()) {
@@ -303,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (n_steps > 0 && warp == 2 && lane == 0) {
     // ===================== TMA producer: dO per step
     QWalk w;
-    w.start(segs, n_segs, p.G);
+    w.start(segs, n_segs, p.G, p.window > 0);
     int ndo = 0;
     bool ok = true;
     for (int i = 0; i < n_steps && ok; ++i, w.next()) {
@@ -422,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* stage_sq = reinterpret_cast<float*>(smem + Lay::kSQ) + hf * Lay::kRowsSQ * D;
     const bool k_ragged = (k_tile + 1) * kTile > p.L;
     QWalk wk;
-    wk.start(segs, n_segs, p.G);
+    wk.start(segs, n_segs, p.G, p.window > 0);
     bool ok = true;
     for (int i = 0; i < n_steps; ++i, wk.next()) {
       const int qs = wk.stream;
