@@ -282,8 +282,6 @@ def launches_per_step(w):
     n_qs = 2 if w.has_clean_queries else 1
     fwd = 1 + ((1 + n_qs * w.batch) if w.P > 1 else 0)   # [fill] + fwd + [merges]
     bwd = n_qs + 1 + n_qs                                  # pre per stream + main + convert
-    if -(-w.L // 128) > 2048:                              # backward in query-tile windows:
-        bwd += 2 + 4                                       # zero dK/dV acc, convert per stream
     return fwd + bwd
 
 

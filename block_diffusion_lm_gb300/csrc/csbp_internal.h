@@ -24,15 +24,12 @@ enum HeaderWord {
 
 csbp_status validate_problem(const csbp_problem* p);
 
-// Backward query-tile window (csbp_problem::bwd_chunk, 0 = default) and
-// whether the problem's backward runs in windows with fp32 dK/dV
-// accumulation: with an explicit window, once a key tile can be read by more
-// query tiles than that; by default (windows of 512) only past 2048 query
-// tiles, where long walks let the CTAs of a wave drift apart (measured: a
-// 1M-token corrupted-only problem gains 3.5 %, a 128K two-copy one loses 5 %
-// with windows).
-constexpr int32_t kDefaultBwdChunk = 512;
-constexpr int32_t kDefaultBwdWindowFrom = 2048;
+// Backward query-tile window (csbp_problem::bwd_chunk) and whether the
+// problem's backward runs in windows with fp32 dK/dV accumulation: only on
+// request (bwd_chunk > 0), once a key tile can be read by more query tiles
+// than that.  With the KV-head-major CTA order long sequences measured
+// faster without windows (a 1M-token corrupted-only backward: 1080 vs 1017
+// TFLOP/s), so the default never windows.
 int64_t bwd_chunk_tiles(const csbp_problem* p);
 bool bwd_windowed(const csbp_problem* p);
 

@@ -140,13 +140,11 @@ csbp_status validate_problem(const csbp_problem* p) {
   return CSBP_OK;
 }
 
-int64_t bwd_chunk_tiles(const csbp_problem* p) {
-  return p->bwd_chunk > 0 ? p->bwd_chunk : kDefaultBwdChunk;
-}
+int64_t bwd_chunk_tiles(const csbp_problem* p) { return p->bwd_chunk; }
 
 bool bwd_windowed(const csbp_problem* p) {
   const int64_t nT = (static_cast<int64_t>(p->L) + p->tile_q - 1) / p->tile_q;
-  return nT > (p->bwd_chunk > 0 ? p->bwd_chunk : kDefaultBwdWindowFrom);
+  return p->bwd_chunk > 0 && nT > p->bwd_chunk;
 }
 
 }  // namespace csbp

@@ -84,16 +84,14 @@ typedef struct {
                            layers, [Blog] "实验数字：256K 上下文下的主结果")      */
   int32_t clean_causal; /* 0: clean queries block-causal over the clean copy;
                            1: token-causal (key j <= query i)             */
-  int32_t bwd_chunk;    /* backward query-tile window, >= 0.  When a key
-                           tile can be read by more query tiles than this,
-                           every backward task covers one window of query
-                           tiles counted from the last tile, the CTAs of a
-                           wave walk the same window, and dK/dV gather in
-                           fp32 workspace accumulators (then bf16).  0: the
-                           library default, windows of 512 once the sequence
-                           has more than 2048 query tiles.  A schedule
-                           setting: results differ only by fp32 summation
-                           order.                                         */
+  int32_t bwd_chunk;    /* backward query-tile window, >= 0 (0: none).
+                           When a key tile can be read by more query tiles
+                           than this, every backward task covers one window
+                           of query tiles counted from the last tile, the
+                           CTAs of a wave walk the same window, and dK/dV
+                           gather in fp32 workspace accumulators (then
+                           bf16).  A schedule setting: results differ only
+                           by fp32 summation order.                      */
 } csbp_problem;
 
 /* Device input tensors, bf16 [batch][L][H][d] contiguous (H = Hq for q,

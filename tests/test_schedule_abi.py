@@ -150,10 +150,15 @@ def test_drafter_schedule_count():
     assert st == -6  # capacity query
     nT = w.L // 128
     assert info.tile_pairs == nT * (nT + 1) // 2 + nT
-    # windows of 512 query tiles: clean key tile kt is read by query tiles
-    # kt .. nT-1, i.e. by ceil((nT - kt) / 512) windows; corrupted key tiles
-    # by their own query tile only
+    assert info.n_bwd_tasks == 2 * nT
+    # with backward windows of 512 query tiles: clean key tile kt is read by
+    # query tiles kt .. nT-1, i.e. by ceil((nT - kt) / 512) windows;
+    # corrupted key tiles by their own query tile only
     c = 512
+    prob.bwd_chunk = c
+    st = csbp.lib().csbp_block_schedule(ctypes.byref(prob), None, None, None, 0,
+                                        ctypes.byref(info))
+    assert st == -6
     assert info.n_bwd_tasks == sum(-(-m // c) for m in range(1, nT + 1)) + nT
     assert info.n_bwd_tasks == c * (nT // c) * (nT // c + 1) // 2 + nT
 
