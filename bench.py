@@ -15,6 +15,13 @@ timed with CUDA events on the launch stream with inputs resident in HBM;
 and the outputs/gradients copied back inside the timed region.
 With N > 1 (torchrun) every rank runs an independent replica of the
 workload on its own GPU (no collective on the data path): weak scaling.
+
+Configs: the attention workloads of inputs.WORKLOADS (default dense14b;
+sharded, long, drafter, window1k, block128 .. block1024, tiny), and the
+LM-head cross-entropy workloads of inputs.CE_WORKLOADS (lmhead14b,
+lmhead_frozen, lmhead_2k), for which one step is one csbp_vocab_ce call
+(loss, dH and dW of every row) and the metric is its TFLOP/s (2 N V Dm per
+GEMM: logits, dH and, for a trained head, dW).
 """
 from __future__ import annotations
 
