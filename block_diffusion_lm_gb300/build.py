@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcsbp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["schedule.cpp", "csbp_api.cu", "attn_fwd.cu", "attn_bwd.cu", "elementwise.cu",
-           "noalloc.cu", "vocab_ce.cu"]
+           "noalloc.cu", "vocab_ce.cu", "selftest.cu"]
 
 
 def nvcc() -> str:

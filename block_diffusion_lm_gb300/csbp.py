@@ -87,12 +87,13 @@ def lib():
         L.csbp_kernel_timing_read.argtypes = [P(ctypes.c_double), P(i32), P(ctypes.c_double),
                                               P(i32)]
         L.csbp_kernel_timing_read_kind.argtypes = [i32, P(ctypes.c_double), P(i32)]
+        L.csbp_wait_selftest.argtypes = [i64, vp, vp]
         L.csbp_ce_workspace_bytes.argtypes = [P(CeProblem)]
         L.csbp_ce_workspace_bytes.restype = sz
         L.csbp_vocab_ce.argtypes = [P(CeProblem), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         for fn in ("csbp_block_schedule", "csbp_attn_fwd", "csbp_attn_bwd", "csbp_lse_merge",
                    "csbp_check_status", "csbp_kernel_timing", "csbp_kernel_timing_read",
-                   "csbp_kernel_timing_read_kind", "csbp_vocab_ce"):
+                   "csbp_kernel_timing_read_kind", "csbp_vocab_ce", "csbp_wait_selftest"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -231,6 +232,12 @@ def lse_merge(o_parts, lse_parts, o_out, lse_out, stream=None):
     st = lib().csbp_lse_merge(n, op, zp, rows, Hq, d, _ptr(o_out), _ptr(lse_out),
                               _stream_ptr(stream))
     _check("csbp_lse_merge", st)
+
+
+def wait_selftest(budget_ns, workspace, stream=None):
+    """Launch the hang-guard self-test (a bounded wait that must give up)."""
+    _check("csbp_wait_selftest",
+           lib().csbp_wait_selftest(int(budget_ns), _ptr(workspace), _stream_ptr(stream)))
 
 
 def check_status(workspace, stream=None):

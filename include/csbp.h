@@ -255,6 +255,16 @@ csbp_status csbp_kernel_timing_read(double* fwd_ms, int32_t* n_fwd, double* bwd_
  * stream).  One event pair per launch.  CSBP_ERR_INVALID for another kind. */
 csbp_status csbp_kernel_timing_read_kind(int32_t kind, double* ms, int32_t* n);
 
+/* Self-test of the device hang guard: launches one small kernel on `stream`
+ * that waits, through the kernels' bounded-wait helpers, on a barrier that
+ * nothing ever arrives on; after budget_ns (1e3 .. 2e9) of wall time the
+ * wait gives up and records a timeout in the status word at the start of
+ * `workspace` (>= 256 bytes, 16-byte aligned, device memory), exactly as a
+ * hung attention or GEMM kernel would.  csbp_check_status then returns
+ * CSBP_ERR_TIMEOUT (and clears the word); nothing else is left in flight, so
+ * the context stays usable.  CSBP_ERR_INVALID for a bad argument. */
+csbp_status csbp_wait_selftest(int64_t budget_ns, void* workspace, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* csbp_status_string(csbp_status status);
 

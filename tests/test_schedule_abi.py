@@ -276,3 +276,12 @@ def test_backward_is_not_windowed_below_the_window():
     assert all(int(words[off_bt + 8 * t + 6]) == 0 for t in range(info.n_bwd_tasks))
     prob.bwd_chunk = -1
     assert csbp.workspace_bytes(prob, 1) == 0
+
+
+def test_wait_selftest_refuses_bad_arguments_without_launching():
+    L = csbp.lib()
+    good = ctypes.c_void_p(0x10000)
+    assert L.csbp_wait_selftest(1_000_000, None, None) == -1          # no workspace
+    assert L.csbp_wait_selftest(1_000_000, ctypes.c_void_p(0x10008), None) == -1  # misaligned
+    assert L.csbp_wait_selftest(10, good, None) == -1                 # budget too short
+    assert L.csbp_wait_selftest(3_000_000_000, good, None) == -1      # budget too long
