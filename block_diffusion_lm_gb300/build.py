@@ -19,6 +19,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcsbp.so")
+# debug variant: kernels validate their work-list records before any access
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libcsbp_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["schedule.cpp", "csbp_api.cu", "attn_fwd.cu", "attn_bwd.cu", "elementwise.cu",
            "noalloc.cu", "vocab_ce.cu", "selftest.cu"]
@@ -37,13 +40,15 @@ def _headers_mtime() -> float:
     return max(os.path.getmtime(h) for h in hs)
 
 
-def _compile(src: str, verbose: bool) -> str:
+def _compile(src: str, verbose: bool, debug: bool = False) -> str:
     path = os.path.join(CSRC, src)
-    obj = os.path.join(BUILD, src.rsplit(".", 1)[0] + ".o")
+    obj = os.path.join(BUILD_DEBUG if debug else BUILD, src.rsplit(".", 1)[0] + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(path), _headers_mtime()):
         return obj
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
            "-I", INCLUDE, "-I", CSRC, "-c", path, "-o", obj]
+    if debug:
+        cmd.insert(1, "-DCSBP_DEBUG_CHECKS")
     if src.endswith(".cu"):
         cmd[1:1] = ["-Xptxas", "-v"] if verbose else []
     else:
@@ -56,19 +61,21 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False) -> str:
-    """Compile and link libcsbp.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, debug: bool = False) -> str:
+    """Compile and link libcsbp.so (or, with debug=True, libcsbp_debug.so,
+    whose kernels check their work-list records); returns its path."""
+    out, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    os.makedirs(out, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose, debug), SOURCES))
+    if not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

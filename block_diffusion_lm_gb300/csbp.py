@@ -57,15 +57,25 @@ class ScheduleInfo(ctypes.Structure):
 
 
 _lib = None
+_lib_path = LIB_PATH
+DEBUG_LIB_PATH = os.path.join(_PKG, "libcsbp_debug.so")
+
+
+def use_library(path: str = LIB_PATH) -> None:
+    """Bind later calls to the library at `path` (e.g. the debug build,
+    DEBUG_LIB_PATH, whose kernels check their work-list records)."""
+    global _lib, _lib_path
+    _lib, _lib_path = None, path
 
 
 def lib():
-    """Load libcsbp.so (raises if it was not built)."""
+    """Load the bound library, libcsbp.so by default (raises if it was not
+    built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} not built: run block_diffusion_lm_gb300.build.build()")
-        L = ctypes.CDLL(LIB_PATH)
+        if not os.path.exists(_lib_path):
+            raise RuntimeError(f"{_lib_path} not built: run block_diffusion_lm_gb300.build.build()")
+        L = ctypes.CDLL(_lib_path)
         P = ctypes.POINTER
         vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         L.csbp_block_schedule.argtypes = [P(Problem), P(i32), P(i32), vp, i64, P(ScheduleInfo)]

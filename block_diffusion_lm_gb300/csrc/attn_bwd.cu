@@ -39,6 +39,7 @@
 
 #include "csbp_internal.h"
 #include "ptx_sm100.cuh"
+#include "work_checks.cuh"
 
 namespace csbp {
 
@@ -262,6 +263,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_segs = tw[4];
   const int n_steps = tw[5] * p.G;
   const bool accumulate = (tw[6] & 1) != 0;  // dK/dV into the fp32 accumulators
+#ifdef CSBP_DEBUG_CHECKS
+  {
+    bool bad = false;
+    if (threadIdx.x == 0) {
+      bad = !task_record_ok(tw, p.segs, p.n_segs, p.nT);
+      if (bad) atomicExch(p.status, DEV_BADWORK);
+    }
+    if (__syncthreads_or(bad)) return;  // nothing issued yet
+  }
+#endif
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C_COUNT; ++i) {

@@ -35,6 +35,7 @@
 
 #include "csbp_internal.h"
 #include "ptx_sm100.cuh"
+#include "work_checks.cuh"
 
 namespace csbp {
 
@@ -185,6 +186,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   auto slot_tiles = [&](int s) { return s < n_slots ? task_words(s)[5] : 0; };
+#ifdef CSBP_DEBUG_CHECKS
+  {
+    bool bad = false;
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < n_slots; ++s)
+        if (!task_record_ok(task_words(s), p.segs, p.n_segs, p.nT)) bad = true;
+      if (bad) atomicExch(p.status, DEV_BADWORK);
+    }
+    if (__syncthreads_or(bad)) return;  // nothing issued yet
+  }
+#endif
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i)

@@ -344,6 +344,8 @@ extern "C" csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inp
   fp.batch = p.batch;
   fp.window = p.window;
   fp.clean_causal = p.clean_causal;
+  fp.n_segs = info->n_fwd_segments;
+  fp.nT = (p.L + kTile - 1) / kTile;
   fp.scale_log2 = p.scale * 1.4426950408889634f;
   fp.o[0] = o_clean;
   fp.o[1] = o_corr;
@@ -460,6 +462,8 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
   bp.batch = p.batch;
   bp.window = p.window;
   bp.clean_causal = p.clean_causal;
+  bp.n_segs = info->n_bwd_segments;
+  bp.nT = (p.L + kTile - 1) / kTile;
   bp.scale_log2 = p.scale * 1.4426950408889634f;
   bp.scale = p.scale;
   bp.dq_acc = dq_acc;
@@ -546,7 +550,8 @@ extern "C" csbp_status csbp_check_status(void* workspace, void* stream) {
     return CSBP_ERR_CUDA;
   if (v != 0) {
     if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return CSBP_ERR_CUDA;
-    return v == 1 ? CSBP_ERR_TIMEOUT : CSBP_ERR_DEVICE;  // device codes: 1 timeout, 2 misaligned
+    // device codes: 1 timeout, 2 misaligned window, 3 bad work record (debug builds)
+    return v == 1 ? CSBP_ERR_TIMEOUT : CSBP_ERR_DEVICE;
   }
   return CSBP_OK;
 }

@@ -57,6 +57,7 @@ struct FwdParams {
   const int32_t* segs;   // device: fwd segment records
   int32_t L, M, Hq, Hkv, G, batch;
   int32_t window, clean_causal;  // mask options (0 = none / block-causal)
+  int32_t n_segs, nT;    // segment records, tiles per copy (debug-build checks)
   float scale_log2;      // softmax scale * log2(e)
   void* o[2];            // bf16 outputs per query stream
   float* lse;            // [batch][2][Hq][L]
@@ -77,6 +78,7 @@ struct BwdParams {
   const int32_t* segs;   // device: bwd segment records
   int32_t L, M, Hq, Hkv, G, batch;
   int32_t window, clean_causal;  // mask options (0 = none / block-causal)
+  int32_t n_segs, nT;    // segment records, tiles per copy (debug-build checks)
   float scale_log2;
   float scale;
   float* dq_acc;         // [2][batch][L][Hq][d] fp32, pre-zeroed

@@ -31,7 +31,7 @@ __device__ __forceinline__ bool elect_one_in_warp() {
 // Status word written by device code when a bounded wait gives up, or when
 // the dynamic shared memory window is not 1024-byte aligned (the kernel then
 // returns without touching memory).
-enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_MISALIGNED = 2 };
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_MISALIGNED = 2, DEV_BADWORK = 3 };
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

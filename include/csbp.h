@@ -227,8 +227,10 @@ csbp_status csbp_lse_merge(int32_t n_parts, const float* const* o_parts,
 /* Synchronise `stream`, then read and clear the device status word kept at
  * the start of `workspace` by csbp_attn_fwd / csbp_attn_bwd.  Returns
  * CSBP_ERR_TIMEOUT if a bounded device wait gave up since the last check,
- * CSBP_ERR_DEVICE if a kernel refused to run (its shared-memory window was
- * not 1024-byte aligned; it then wrote nothing). */
+ * CSBP_ERR_DEVICE if a kernel refused to run: its shared-memory window was
+ * not 1024-byte aligned, or (debug build, libcsbp_debug.so) a work-list
+ * record it was given points outside the list or the sequence; such a CTA
+ * writes nothing. */
 csbp_status csbp_check_status(void* workspace, void* stream);
 
 /* Kernel timing, a profiling aid with no counterpart in the method; off by

@@ -285,3 +285,17 @@ def test_wait_selftest_refuses_bad_arguments_without_launching():
     assert L.csbp_wait_selftest(1_000_000, ctypes.c_void_p(0x10008), None) == -1  # misaligned
     assert L.csbp_wait_selftest(10, good, None) == -1                 # budget too short
     assert L.csbp_wait_selftest(3_000_000_000, good, None) == -1      # budget too long
+
+
+def test_entry_points_refuse_a_small_workspace_without_launching():
+    L = csbp.lib()
+    prob = csbp.make_problem(1, 1024, 64, 2, 2, 64, P=2)
+    _, _, _, info = csbp.block_schedule(prob)
+    g = ctypes.c_void_p(0x10000)
+    inp = csbp.Inputs(g, g, g, g, g, g)
+    need_f, need_b = csbp.workspace_bytes(prob, 0), csbp.workspace_bytes(prob, 1)
+    assert need_f > 0 and need_b > 0
+    assert L.csbp_attn_fwd(ctypes.byref(prob), ctypes.byref(inp), g, ctypes.byref(info),
+                           g, g, g, g, need_f - 1, None) == -3
+    assert L.csbp_attn_bwd(ctypes.byref(prob), ctypes.byref(inp), g, ctypes.byref(info),
+                           *([g] * 12), need_b - 1, None) == -3
