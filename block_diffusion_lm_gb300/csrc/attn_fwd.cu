@@ -385,17 +385,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           hi -= w.t * kTile;
 #pragma unroll
           for (int c = 0; c < kTile; ++c) {
-            sv[c] = (c >= lo && c < hi) ? sv[c] * sl2 : -INFINITY;
+            sv[c] = (c >= lo && c < hi) ? sv[c] : -INFINITY;
             mx = fmaxf(mx, sv[c]);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < kTile; ++c) {
-            sv[c] *= sl2;
-            mx = fmaxf(mx, sv[c]);
-          }
+          for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, sv[c]);
         }
-        const float m_new = fmaxf(m_ref, mx);
+        // scores stay unscaled: the scale is positive, so the row max of the
+        // scaled scores is the scaled max, and each exponent below takes the
+        // scale in one fused multiply-add
+        const float m_new = fmaxf(m_ref, mx * sl2);
         const bool need = m_new > m_ref + kRescaleThreshold;  // false while both are -inf
         if (j > 0 && __any_sync(0xffffffffu, need)) {
           // O holds PV_0..PV_{j-1} scaled by the old reference; PV_{j-1} is
@@ -421,8 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float packed[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float e0 = ex2_approx(sv[half * 64 + 2 * c] - mref_safe);
-            const float e1 = ex2_approx(sv[half * 64 + 2 * c + 1] - mref_safe);
+            const float e0 = ex2_approx(fmaf(sv[half * 64 + 2 * c], sl2, -mref_safe));
+            const float e1 = ex2_approx(fmaf(sv[half * 64 + 2 * c + 1], sl2, -mref_safe));
             rs += e0 + e1;
             packed[c] = __uint_as_float(pack_bf16x2(e0, e1));
           }
