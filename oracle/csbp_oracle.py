@@ -294,10 +294,14 @@ def lse_merge_pair(o1, z1, o2, z2):
 
 
 def lse_merge(o_parts, z_parts):
-    """Merge n partials by applying the two-part merge left to right."""
+    """Merge n partials by applying the two-part merge left to right.  A row
+    that no part read a key for (every z = -inf) merges to O = 0, z = -inf,
+    the two-part rule's convention, also when n = 1."""
     o, z = np.asarray(o_parts[0], np.float64), np.asarray(z_parts[0], np.float64)
     for s in range(1, len(o_parts)):
         o, z = lse_merge_pair(o, z, np.asarray(o_parts[s], np.float64), z_parts[s])
+    empty = ~np.isfinite(z)
+    o = np.where(empty.reshape((-1,) + (1,) * (np.ndim(o) - 1)), 0.0, o)
     return o, z
 
 

@@ -253,3 +253,32 @@ def test_full_size_workloads_sampled(name, rows, keys, seed):
     _sampled_check(w, t, out, g, rows, keys, seed=seed)
     del t, out, g
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n,rows,Hq,d", [(1, 300, 2, 64), (2, 257, 4, 128), (3, 128, 1, 128),
+                                         (9, 1000, 2, 64)])
+def test_lse_merge_entry_point_matches_oracle(n, rows, Hq, d):
+    """csbp_lse_merge on its own: n fp32 partials with random LSEs, some parts
+    empty for some rows (z = -inf) and row 0 empty in every part, against the
+    oracle's two-part merge folded over the parts."""
+    g = torch.Generator().manual_seed(100 * n + rows)
+    o_parts = [torch.randn(rows, Hq, d, generator=g) for _ in range(n)]
+    z_parts = [3.0 * torch.randn(Hq, rows, generator=g) for _ in range(n)]
+    for z in z_parts:
+        z[torch.rand(Hq, rows, generator=g) < 0.2] = float("-inf")
+        z[:, 0] = float("-inf")
+    o_out = torch.empty(rows, Hq, d, dtype=torch.bfloat16, device="cuda")
+    z_out = torch.empty(Hq, rows, dtype=torch.float32, device="cuda")
+    csbp.lse_merge([o.cuda() for o in o_parts], [z.cuda() for z in z_parts], o_out, z_out)
+    torch.cuda.synchronize()
+    ref_o, ref_z = O.lse_merge([o.double().numpy().reshape(rows * Hq, d) for o in o_parts],
+                               [z.double().numpy().T.reshape(rows * Hq) for z in z_parts])
+    got_o = to_f64(o_out).reshape(rows * Hq, d)
+    got_z = to_f64(z_out).T.reshape(rows * Hq)
+    # bf16 output: rounding grows with |O|, which reaches ~4.5 for these
+    # unit-normal partials (attention outputs stay near 1)
+    assert np.all(np.abs(got_o - ref_o) <= TOL_O + 2.0 ** -8 * np.abs(ref_o))
+    finite = np.isfinite(ref_z)
+    assert np.array_equal(finite, np.isfinite(got_z))
+    assert np.abs(got_z[finite] - ref_z[finite]).max() <= 1e-5 * max(1.0, np.abs(ref_z[finite]).max())
+    assert np.all(got_o[~finite] == 0)

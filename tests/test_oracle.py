@@ -419,3 +419,19 @@ def test_pins_catch_planted_backward_mistake(monkeypatch):
                            t["doc"], t["dox"], M, 0.5)
     dk = g["dk_clean"].sum(0) + g["dk_corr"].sum(0)
     assert np.abs(dk).max() > 1e-3
+
+
+def test_lse_merge_of_parts_that_read_no_key():
+    """A row every part left empty (z = -inf) merges to O = 0, z = -inf for
+    any number of parts, as the two-part merge defines it; one empty part
+    among others has weight 0."""
+    o = np.array([[1.0, 2.0], [3.0, 4.0]])
+    z = np.array([-np.inf, 0.5])
+    for n in (1, 2, 3):
+        om, zm = O.lse_merge([o] * n, [z] * n)
+        assert np.all(om[0] == 0) and zm[0] == -np.inf
+        np.testing.assert_allclose(om[1], o[1])
+        np.testing.assert_allclose(zm[1], 0.5 + np.log(n))
+    om, zm = O.lse_merge([o, 5 * o], [np.array([-np.inf, -np.inf]), z])
+    np.testing.assert_allclose(om[1], 5 * o[1])
+    assert zm[1] == 0.5
