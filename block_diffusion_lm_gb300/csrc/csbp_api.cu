@@ -282,7 +282,7 @@ extern "C" csbp_status csbp_kernel_timing_read_kind(int32_t kind, double* ms, in
   return CSBP_OK;
 }
 
-extern "C" int32_t csbp_version(void) { return 100; }
+extern "C" int32_t csbp_version(void) { return 200; }  // 0.2.0: mask options, backward windows, vocabulary loss, self-test
 
 extern "C" const char* csbp_status_string(csbp_status s) {
   switch (s) {

@@ -270,7 +270,9 @@ csbp_status csbp_wait_selftest(int64_t budget_ns, void* workspace, void* stream)
 /* Human-readable name of a status code (static string). */
 const char* csbp_status_string(csbp_status status);
 
-/* Library version: major * 10000 + minor * 100 + patch. */
+/* Library version: major * 10000 + minor * 100 + patch.  0.2.0 (200) added
+ * csbp_problem.window / clean_causal / bwd_chunk, csbp_vocab_ce (with
+ * csbp_vocab_ce.h), csbp_wait_selftest and csbp_kernel_timing_read_kind. */
 int32_t csbp_version(void);
 
 #ifdef __cplusplus

@@ -59,7 +59,7 @@ def test_library_exports_every_declared_symbol():
                           "csbp_lse_merge"}
     for n in names:
         assert hasattr(L, n), n
-    assert L.csbp_version() >= 100
+    assert L.csbp_version() >= 200
     for code, name in csbp.STATUS.items():
         assert L.csbp_status_string(code)
 
