@@ -11,8 +11,9 @@
 // 为什么会传错东西" section of the same blog: a corrupted query of block b reads
 // its own block's corrupted keys and the clean keys of blocks < b; clean
 // queries read clean keys of blocks <= b).  Classification of a tile pair is
-// analytic on block-id intervals, so building the list is O(tiles^2) integer
-// work with no mask materialised.
+// analytic on block-id intervals, and each tile's candidates are the span
+// between its first and last position's allowed ranges, so building the list
+// costs about one classification per listed pair, with no mask materialised.
 #include <algorithm>
 #include <cstring>
 #include <vector>
@@ -42,6 +43,44 @@ void key_range(int q_stream, int k_stream, int64_t i, int64_t L, int64_t M, int6
     hi = std::min((b + 1) * M, L);
   }
   if (window > 0) lo = std::max(lo, i - window + 1);
+}
+
+// Allowed query positions [lo, hi) of copy q_stream that may read key
+// position j of copy k_stream (the transpose of key_range); both bounds are
+// non-decreasing in j.
+void query_range(int q_stream, int k_stream, int64_t j, int64_t L, int64_t M, int64_t window,
+                 bool clean_causal, int64_t& lo, int64_t& hi) {
+  const int64_t b = j / M;
+  hi = L;
+  if (q_stream == 0 && k_stream == 1) {
+    lo = hi = 0;
+    return;
+  }
+  if (k_stream == 0) {
+    lo = (q_stream == 0) ? (clean_causal ? j : b * M) : (b + 1) * M;
+  } else {
+    lo = b * M;
+    hi = std::min((b + 1) * M, L);
+  }
+  if (window > 0) hi = std::min(hi, j + window);
+}
+
+// Tiles of the other copy that can hold an allowed entry for tile t: the
+// first position's lower bound to the last position's upper bound (both
+// bounds are non-decreasing, so every position's range lies inside), as a
+// half-open tile range [a, b).
+template <typename RangeFn>
+void tile_span(RangeFn range, int64_t t, int64_t L, int64_t T, int64_t& a, int64_t& b) {
+  const int64_t p0 = t * T, p1 = std::min(p0 + T, L) - 1;
+  int64_t lo0, hi0, lo1, hi1;
+  range(p0, lo0, hi0);
+  range(p1, lo1, hi1);
+  if (p0 > p1 || hi1 <= lo0) {
+    a = b = 0;
+    return;
+  }
+  a = lo0 / T;
+  b = (hi1 - 1) / T + 1;
 }
 
 // 0 = no allowed entry, 1 = some (partial), 2 = all entries allowed; from the
@@ -201,7 +240,12 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
       std::vector<Seg> segs;
       std::vector<int32_t> seg_part;
       for (int ks = 0; ks < 2; ++ks) {
-        for (int64_t kt = 0; kt < nT; ++kt) {
+        int64_t ka, kb;
+        tile_span([&](int64_t i, int64_t& lo, int64_t& hi) {
+                    key_range(qs, ks, i, L, M, W, causal, lo, hi);
+                  },
+                  qt, L, T, ka, kb);
+        for (int64_t kt = ka; kt < kb; ++kt) {
           const int cls = classify(qs, qt, ks, kt);
           if (!cls) continue;
           ++pairs;
@@ -243,8 +287,12 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
       Task t{ks, (int32_t)kt, (ks == 1) ? P : clean_part(kt * T), {}, 0, 0};
       std::vector<int32_t> dummy_part;
       for (int qs = q_stream0; qs < 2; ++qs) {
-        // only a band of query tiles can read key tile kt; scan all for clarity
-        for (int64_t qt = 0; qt < nT; ++qt) {
+        int64_t qa, qb;
+        tile_span([&](int64_t j, int64_t& lo, int64_t& hi) {
+                    query_range(qs, ks, j, L, M, W, causal, lo, hi);
+                  },
+                  kt, L, T, qa, qb);
+        for (int64_t qt = qa; qt < qb; ++qt) {
           const int cls = classify(qs, qt, ks, kt);
           if (!cls) continue;
           push_tile(t.segs, dummy_part, qs, (int32_t)qt, cls, 0);
