@@ -505,10 +505,13 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
-    from block_diffusion_lm_gb300.inputs import CE_WORKLOADS
+    from block_diffusion_lm_gb300.inputs import CE_WORKLOADS, WORKLOADS
     if args.config in CE_WORKLOADS:
         bench_ce(args, CE_WORKLOADS[args.config], rank, world, local)
         return
+    if args.config not in WORKLOADS:
+        sys.exit(f"unknown --config {args.config!r}; choose one of "
+                 f"{', '.join(sorted(WORKLOADS) + sorted(CE_WORKLOADS))}")
 
     import dataclasses
 
