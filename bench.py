@@ -337,6 +337,8 @@ def bench_ce(args, w, rank, world, local):
     if args.impl == "reference":
         if rank != 0:
             return
+        for _ in range(args.warmup):
+            ce_cpu_oracle_sample(w, 2.0)
         steps = [ce_cpu_oracle_sample(w, max(2.0, args.cpu_seconds / max(args.steps, 1)))
                  for _ in range(args.steps)]
         v = statistics.median(s["value"] for s in steps)

@@ -1,8 +1,9 @@
 """Pins for the oracle's sliding-window and token-causal clean options, against
-facts that do not come from the oracle: reductions to textbook causal and
-sliding-window attention (torch SDPA in float64 with a band mask built from
-triangles), a window too wide to matter, a one-token window, finite
-differences, and a planted off-by-one window that the SDPA pin must catch.
+facts that do not come from the oracle: a mask worked out by hand, reductions
+to textbook causal and sliding-window attention (torch SDPA in float64 with a
+band mask built from triangles), a window too wide to matter, a one-token
+window, finite differences, and a planted off-by-one window that the SDPA pin
+must catch.
 
 Reading (where the pages only name 1,024-token sliding-window layers): a
 window W keeps, of the keys the block rules allow, those less than W positions
@@ -13,6 +14,7 @@ import pytest
 import torch
 
 from oracle import csbp_oracle as O
+from conftest import read_golden
 
 
 def make(L, Hq, Hkv, d, seed=0, clean=True):
@@ -35,6 +37,23 @@ def sdpa(q, k, v, mask, scale):
     return torch.nn.functional.scaled_dot_product_attention(
         torch.from_numpy(q)[None], torch.from_numpy(k)[None], torch.from_numpy(v)[None],
         attn_mask=mask[None], scale=scale)[0].numpy()
+
+
+def test_windowed_masks_match_hand_written_fixture():
+    """Both clean-query variants, every scalar predicate and every row agree
+    with a mask worked out by hand (L=8, M=4, W=3)."""
+    rows = read_golden("mask_L8_M4_W3.txt")
+    want = np.array([[c == "1" for c in r.replace(" ", "")] for r in rows])
+    assert want.shape == (32, 16)
+    for k, causal in enumerate((False, True)):
+        ref = want[16 * k:16 * (k + 1)]
+        np.testing.assert_array_equal(O.bd_mask(8, 4, 3, causal), ref)
+        for qs in (0, 1):
+            for i in range(8):
+                np.testing.assert_array_equal(O.mask_row(qs, i, 8, 4, 3, causal), ref[qs * 8 + i])
+                for ks in (0, 1):
+                    for j in range(8):
+                        assert O.allowed(qs, i, ks, j, 4, 3, causal) == ref[qs * 8 + i, ks * 8 + j]
 
 
 @pytest.mark.parametrize("W", [1, 3, 7, 40])

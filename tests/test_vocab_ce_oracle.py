@@ -1,5 +1,5 @@
 """Pins for the LM-head cross-entropy oracle, against facts that do not come
-from the oracle: torch's own cross-entropy and autograd in float64, the
+from the oracle: a three-row example worked by hand, torch's own cross-entropy and autograd in float64, the
 zero-head closed form, shift invariance, exact invariants, central finite
 differences, ignored rows, and a planted mistake the torch pin must catch."""
 import numpy as np
@@ -7,6 +7,7 @@ import pytest
 import torch
 
 from oracle import vocab_ce_oracle as C
+from conftest import read_golden
 
 
 def make(N, Dm, V, seed, ignore=0.0, sigma=None):
@@ -37,6 +38,25 @@ def test_matches_torch_cross_entropy_and_autograd(N, Dm, V, ignore, head):
         np.testing.assert_allclose(dW, Wt.grad.numpy(), atol=1e-12)
     else:
         assert dW is None
+
+
+def test_matches_hand_worked_fixture():
+    """Three rows (one ignored) over a three-word vocabulary whose logits are
+    logs of small integers, worked out by hand."""
+    lines = [[float(x) for x in ln.split()] for ln in read_golden("vocab_ce_three_rows.txt")]
+    W = np.array(lines[0])[:, None]
+    s = lines[1][0]
+    rows = np.array(lines[2:5])
+    H, t = rows[:, :1], rows[:, 1].astype(np.int64)
+    loss, lse, dH, dW = C.vocab_ce(H, W, t, s)
+    np.testing.assert_allclose(lse, rows[:, 2], atol=1e-14)
+    np.testing.assert_allclose(loss, rows[:, 3], atol=1e-14)
+    np.testing.assert_allclose(dH[:, 0], rows[:, 4], atol=1e-14)
+    np.testing.assert_allclose(dW[:, 0], lines[5], atol=1e-14)
+    l2, z2, d2 = C.vocab_ce_rows(H, W, t, s, [2, 0])
+    np.testing.assert_allclose(z2, rows[[2, 0], 2], atol=1e-14)
+    np.testing.assert_allclose(l2, rows[[2, 0], 3], atol=1e-14)
+    np.testing.assert_allclose(d2[:, 0], rows[[2, 0], 4], atol=1e-14)
 
 
 def test_zero_head_closed_form():
