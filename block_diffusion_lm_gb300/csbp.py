@@ -186,6 +186,54 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+class _Checks:
+    """Refuse tensors the library would misread: the C ABI sees only
+    pointers, so dtype, shape and contiguity of every argument are checked
+    first, then (in `done`) that all of them are on a CUDA device."""
+
+    def __init__(self, fn):
+        self.fn = fn
+        self.seen = []
+
+    def tensor(self, name, t, dtype, shape, required=True):
+        fn = self.fn
+        if t is None:
+            if required:
+                raise ValueError(f"{fn}: {name} is required")
+            return
+        if t.dtype != dtype:
+            raise ValueError(f"{fn}: {name} must be {dtype}, got {t.dtype}")
+        if shape is not None and tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{fn}: {name} must have shape {tuple(shape)}, "
+                             f"got {tuple(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{fn}: {name} must be contiguous")
+        self.seen.append((name, t))
+
+    def attn(self, problem, tensors):
+        """q/o/dq/dO bf16 [batch][L][Hq][d], k/v/dk/dv bf16 [batch][L][Hkv][d],
+        lse fp32 [batch][2][Hq][L]; clean-query tensors are optional when the
+        problem has no clean queries."""
+        import torch
+        q = (problem.batch, problem.L, problem.Hq, problem.d)
+        kv = (problem.batch, problem.L, problem.Hkv, problem.d)
+        for name, t in tensors.items():
+            if name == "lse":
+                self.tensor(name, t, torch.float32, (problem.batch, 2, problem.Hq, problem.L))
+                continue
+            key_side = name.startswith(("k_", "v_", "dk_", "dv_"))
+            optional = not key_side and name.endswith("_clean") and not problem.has_clean_queries
+            self.tensor(name, t, torch.bfloat16, kv if key_side else q, required=not optional)
+
+    def done(self):
+        for name, t in self.seen:
+            if not t.is_cuda:
+                raise ValueError(f"{self.fn}: {name} must be a CUDA tensor")
+
+
+_INPUT_NAMES = ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")
+
+
 def _stream_ptr(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -193,8 +241,14 @@ def _stream_ptr(stream):
 
 
 def attn_fwd(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse, workspace, stream=None):
-    inp = Inputs(*(_ptr(inputs.get(n)) for n in
-                   ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")))
+    import torch
+    c = _Checks("csbp_attn_fwd")
+    c.attn(problem, {**{n: inputs.get(n) for n in _INPUT_NAMES},
+                     "o_clean": o_clean, "o_corr": o_corr, "lse": lse})
+    c.tensor("work", work_dev, torch.int32, None)
+    c.tensor("workspace", workspace, torch.uint8, None)
+    c.done()
+    inp = Inputs(*(_ptr(inputs.get(n)) for n in _INPUT_NAMES))
     st = lib().csbp_attn_fwd(ctypes.byref(problem), ctypes.byref(inp), _ptr(work_dev),
                              ctypes.byref(info), _ptr(o_clean), _ptr(o_corr), _ptr(lse),
                              _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -202,10 +256,24 @@ def attn_fwd(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse, worksp
     _check("csbp_attn_fwd", st)
 
 
+def _check_bwd(c, problem, inputs, work_dev, o_clean, o_corr, lse, do_clean, do_corr, grads):
+    import torch
+    names = ("dq_clean", "dq_corr", "dk_clean", "dv_clean", "dk_corr", "dv_corr")
+    c.attn(problem, {**{n: inputs.get(n) for n in _INPUT_NAMES},
+                     "o_clean": o_clean, "o_corr": o_corr, "lse": lse,
+                     "do_clean": do_clean, "do_corr": do_corr,
+                     **{n: grads.get(n) for n in names}})
+    c.tensor("work", work_dev, torch.int32, None)
+
+
 def attn_bwd(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse, do_clean, do_corr,
              grads: dict, workspace, stream=None):
-    inp = Inputs(*(_ptr(inputs.get(n)) for n in
-                   ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")))
+    import torch
+    c = _Checks("csbp_attn_bwd")
+    _check_bwd(c, problem, inputs, work_dev, o_clean, o_corr, lse, do_clean, do_corr, grads)
+    c.tensor("workspace", workspace, torch.uint8, None)
+    c.done()
+    inp = Inputs(*(_ptr(inputs.get(n)) for n in _INPUT_NAMES))
     st = lib().csbp_attn_bwd(ctypes.byref(problem), ctypes.byref(inp), _ptr(work_dev),
                              ctypes.byref(info), _ptr(o_clean), _ptr(o_corr), _ptr(lse),
                              _ptr(do_clean), _ptr(do_corr), _ptr(grads.get("dq_clean")),
@@ -221,8 +289,10 @@ def attn_bwd_noalloc(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse
     """csbp_attn_bwd_noalloc: the backward with the library's own fixed
     scratch instead of a caller workspace (for callers that cannot allocate
     device memory; calls on one device must not overlap)."""
-    inp = Inputs(*(_ptr(inputs.get(n)) for n in
-                   ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")))
+    c = _Checks("csbp_attn_bwd_noalloc")
+    _check_bwd(c, problem, inputs, work_dev, o_clean, o_corr, lse, do_clean, do_corr, grads)
+    c.done()
+    inp = Inputs(*(_ptr(inputs.get(n)) for n in _INPUT_NAMES))
     st = lib().csbp_attn_bwd_noalloc(ctypes.byref(problem), ctypes.byref(inp), _ptr(work_dev),
                                      ctypes.byref(info), _ptr(o_clean), _ptr(o_corr), _ptr(lse),
                                      _ptr(do_clean), _ptr(do_corr), _ptr(grads.get("dq_clean")),
@@ -235,8 +305,18 @@ def attn_bwd_noalloc(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse
 def lse_merge(o_parts, lse_parts, o_out, lse_out, stream=None):
     """o_parts: list of fp32 [rows, Hq, d] device tensors; lse_parts: list of
     fp32 [Hq, rows]; o_out bf16 [rows, Hq, d]; lse_out fp32 [Hq, rows]."""
+    import torch
+    c = _Checks("csbp_lse_merge")
     n = len(o_parts)
+    if n < 1 or len(lse_parts) != n:
+        raise ValueError("csbp_lse_merge: needs one LSE part per output part, at least one")
     rows, Hq, d = o_parts[0].shape
+    for s, (o, z) in enumerate(zip(o_parts, lse_parts)):
+        c.tensor(f"o_parts[{s}]", o, torch.float32, (rows, Hq, d))
+        c.tensor(f"lse_parts[{s}]", z, torch.float32, (Hq, rows))
+    c.tensor("o_out", o_out, torch.bfloat16, (rows, Hq, d))
+    c.tensor("lse_out", lse_out, torch.float32, (Hq, rows))
+    c.done()
     op = (ctypes.c_void_p * n)(*[t.data_ptr() for t in o_parts])
     zp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in lse_parts])
     st = lib().csbp_lse_merge(n, op, zp, rows, Hq, d, _ptr(o_out), _ptr(lse_out),
@@ -325,6 +405,21 @@ def ce_workspace_bytes(problem: CeProblem) -> int:
 
 
 def vocab_ce(problem, h, w, target, loss, lse, dh, dw, workspace, stream=None):
+    import torch
+    c = _Checks("csbp_vocab_ce")
+    N, Dm, V = problem.rows, problem.d_model, problem.vocab
+    c.tensor("h", h, torch.bfloat16, (N, Dm))
+    c.tensor("w", w, torch.bfloat16, (V, Dm))
+    c.tensor("target", target, torch.int32, (N,))
+    c.tensor("loss", loss, torch.float32, (N,))
+    c.tensor("lse", lse, torch.float32, (N,))
+    c.tensor("dh", dh, torch.bfloat16, (N, Dm))
+    if problem.head_grad:
+        c.tensor("dw", dw, torch.float32, (V, Dm))
+    elif dw is not None:
+        raise ValueError("csbp_vocab_ce: dw must be None for a frozen head")
+    c.tensor("workspace", workspace, torch.uint8, None)
+    c.done()
     st = lib().csbp_vocab_ce(ctypes.byref(problem), _ptr(h), _ptr(w), _ptr(target), _ptr(loss),
                              _ptr(lse), _ptr(dh), _ptr(dw), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream_ptr(stream))

@@ -1,0 +1,111 @@
+"""The Python binding refuses tensors the C ABI would misread (it sees only
+pointers): wrong dtype, wrong shape or layout, non-contiguous, or host
+memory.  Every check runs before the library is called, so these tests need
+no GPU."""
+import pytest
+import torch
+
+from block_diffusion_lm_gb300 import csbp
+from block_diffusion_lm_gb300.inputs import WORKLOADS, make_inputs
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from block_diffusion_lm_gb300 import build
+    build.build()
+
+
+def attn_case(has_clean=True):
+    w = WORKLOADS["tiny"]
+    attn = csbp.BlockDiffusionAttention(w.batch, w.L, w.M, w.Hq, w.Hkv, w.d,
+                                        has_clean_queries=has_clean, device="cpu")
+    t = make_inputs(w, "cpu")
+    if not has_clean:
+        t["q_clean"] = t["do_clean"] = None
+    return attn, t
+
+
+def test_host_tensors_are_refused():
+    attn, t = attn_case()
+    with pytest.raises(ValueError, match="q_clean must be a CUDA tensor"):
+        attn.forward(t)
+
+
+@pytest.mark.parametrize("name,bad,msg", [
+    ("q_corr", lambda x: x.float(), "q_corr must be torch.bfloat16"),
+    ("k_clean", lambda x: x.transpose(1, 2).contiguous(), "k_clean must have shape"),
+    ("v_corr", lambda x: x.transpose(1, 2).contiguous().transpose(1, 2), "v_corr must be contiguous"),
+    ("q_clean", lambda x: None, "q_clean is required"),
+])
+def test_forward_inputs_are_checked(name, bad, msg):
+    attn, t = attn_case()
+    t[name] = bad(t[name])
+    with pytest.raises(ValueError, match=msg):
+        attn.forward(t)
+
+
+def test_forward_outputs_are_checked():
+    attn, t = attn_case()
+    oc, ox, lse = attn.alloc_outputs()
+    with pytest.raises(ValueError, match="lse must have shape"):
+        attn.forward(t, out=(oc, ox, lse[:, :1].contiguous()))
+    with pytest.raises(ValueError, match="o_corr must be torch.bfloat16"):
+        attn.forward(t, out=(oc, ox.float(), lse))
+
+
+def test_backward_gradients_are_checked():
+    attn, t = attn_case()
+    out = attn.alloc_outputs()
+    g = attn.alloc_grads()
+    g["dk_corr"] = g["dk_corr"][:, :-1].contiguous()
+    with pytest.raises(ValueError, match="dk_corr must have shape"):
+        attn.backward(t, out, grads=g)
+    g = attn.alloc_grads()
+    t["do_corr"] = None
+    with pytest.raises(ValueError, match="do_corr is required"):
+        attn.backward(t, out, grads=g)
+
+
+def test_clean_query_tensors_are_optional_without_clean_queries():
+    """Without clean queries the clean-query tensors may be None; the clean
+    K/V (read by the corrupted queries) are still required.  Validation then
+    gets as far as the device check of the first tensor it meets."""
+    attn, t = attn_case(has_clean=False)
+    with pytest.raises(ValueError, match="k_clean must be a CUDA tensor"):
+        attn.forward(t)
+    t["k_clean"] = None
+    with pytest.raises(ValueError, match="k_clean is required"):
+        attn.forward(t)
+
+
+def test_lse_merge_arguments_are_checked():
+    o = [torch.zeros(10, 2, 64), torch.zeros(10, 2, 64)]
+    z = [torch.zeros(2, 10), torch.zeros(2, 10)]
+    o_out = torch.zeros(10, 2, 64, dtype=torch.bfloat16)
+    z_out = torch.zeros(2, 10)
+    with pytest.raises(ValueError, match="one LSE part per output part"):
+        csbp.lse_merge(o, z[:1], o_out, z_out)
+    with pytest.raises(ValueError, match=r"lse_parts\[1\] must have shape"):
+        csbp.lse_merge(o, [z[0], z[1].T.contiguous()], o_out, z_out)
+    with pytest.raises(ValueError, match="o_out must be torch.bfloat16"):
+        csbp.lse_merge(o, z, o_out.float(), z_out)
+    with pytest.raises(ValueError, match=r"o_parts\[0\] must be a CUDA tensor"):
+        csbp.lse_merge(o, z, o_out, z_out)
+
+
+def test_vocab_ce_arguments_are_checked():
+    N, Dm, V = 130, 64, 256
+    ce = csbp.VocabCrossEntropy(N, Dm, V, device="cpu")
+    h = torch.zeros(N, Dm, dtype=torch.bfloat16)
+    w = torch.zeros(V, Dm, dtype=torch.bfloat16)
+    tgt = torch.zeros(N, dtype=torch.int32)
+    with pytest.raises(ValueError, match="target must be torch.int32"):
+        ce(h, w, tgt.long())
+    with pytest.raises(ValueError, match="w must have shape"):
+        ce(h, w.T.contiguous(), tgt)
+    with pytest.raises(ValueError, match="h must be a CUDA tensor"):
+        ce(h, w, tgt)
+    frozen = csbp.VocabCrossEntropy(N, Dm, V, head_grad=False, device="cpu")
+    loss, lse, dh, _ = frozen.alloc_outputs()
+    with pytest.raises(ValueError, match="dw must be None for a frozen head"):
+        frozen(h, w, tgt, out=(loss, lse, dh, torch.zeros(V, Dm)))
