@@ -12,12 +12,16 @@ head is frozen):
 
     z_i      = W h_i                         logits of row i over the vocabulary
     lse_i    = log sum_v exp(z_iv)
-    loss_i   = lse_i - z_{i, t_i}            (0 for an ignored row, t_i < 0)
+    loss_i   = lse_i - z_{i, t_i}            (0 for an ignored row: t_i outside [0, V))
     g_i      = s (softmax(z_i) - e_{t_i})     (0 for an ignored row)
     dH_i     = g_i W                          gradient of s * sum_i loss_i
     dW       = sum_i g_i^T h_i                (only when the head is trained)
 
 with s the caller's gradient scale (for example 1 / number of counted rows).
+The pages give no target encoding.  The reading here is the usual
+ignore-index convention, widened to every value outside [0, V): negative
+targets (padding, the clean half of a block-diffusion sequence) and any
+target past the vocabulary.
 
 The chunking is a memory schedule, not part of the arithmetic, so the oracle
 has none.  Every row's outputs depend on that row alone, which is what lets
@@ -28,7 +32,7 @@ import numpy as np
 
 def vocab_ce(H, W, target, grad_scale, head_grad=True):
     """Loss, LSE, dH and (optionally) dW for rows H [N, Dm] against the head
-    W [V, Dm] with integer targets [N] (negative = ignored row).
+    W [V, Dm] with integer targets [N] (outside [0, V) = ignored row).
 
     Returns (loss [N], lse [N], dH [N, Dm], dW [V, Dm] or None), float64.
     """
@@ -39,7 +43,7 @@ def vocab_ce(H, W, target, grad_scale, head_grad=True):
     Z = H @ W.T
     m = Z.max(axis=1, keepdims=True)
     lse = (m + np.log(np.exp(Z - m).sum(axis=1, keepdims=True)))[:, 0]
-    valid = t >= 0
+    valid = (t >= 0) & (t < W.shape[0])
     rows = np.arange(n)
     zt = np.where(valid, Z[rows, np.where(valid, t, 0)], 0.0)
     loss = np.where(valid, lse - zt, 0.0)

@@ -79,6 +79,30 @@ def test_small_cases_match_oracle_elementwise(w):
         assert dw is None
 
 
+def test_targets_outside_the_vocabulary_are_ignored():
+    """Targets past the vocabulary (V, V + 100, INT32_MAX) and negative ones
+    other than -1 mark ignored rows, as the header states."""
+    w = CeWorkload("ce_out_of_range", 300, 128, 1024, seed=2030)
+    x = make_ce_inputs(w, "cuda")
+    tgt = x["target"]
+    tgt[::7] = w.V
+    tgt[3::11] = w.V + 100
+    tgt[5] = 2 ** 31 - 1
+    tgt[6] = -(2 ** 31)
+    ce = csbp.VocabCrossEntropy(w.N, w.Dm, w.V, w.chunk, True, x["grad_scale"])
+    loss, lse, dh, dw = ce(x["h"], x["w"], tgt)
+    ce.check()
+    torch.cuda.synchronize()
+    t = tgt.cpu().numpy()
+    rl, rz, rdh, rdw = C.vocab_ce(f64(x["h"]), f64(x["w"]), t, x["grad_scale"])
+    ignored = (t < 0) | (t >= w.V)
+    assert np.all(f64(loss)[ignored] == 0) and np.all(f64(dh)[ignored] == 0)
+    assert np.abs(f64(loss) - rl).max() <= TOL_LOSS
+    assert np.abs(f64(lse) - rz).max() <= TOL_LOSS
+    close(f64(dh), rdh, "dh")
+    close(f64(dw), rdw, "dw")
+
+
 def test_chunking_changes_nothing_per_row():
     """Rows are independent: loss, LSE and dH are bit-identical whatever the
     chunk size; dW differs only by fp32 summation order across chunks."""

@@ -135,6 +135,22 @@ def test_ignored_rows_contribute_nothing():
     np.testing.assert_allclose(dW, dW_keep, atol=1e-13)
 
 
+def test_targets_past_the_vocabulary_are_ignored_rows():
+    """A target >= V reads as an ignored row: the same outputs as target -1,
+    and dW as if the row were absent."""
+    H, W, t = make(20, 6, 30, seed=12)
+    a, b = t.copy(), t.copy()
+    a[[2, 9, 17]] = [30, 31, 10 ** 6]
+    b[[2, 9, 17]] = -1
+    ra = C.vocab_ce(H, W, a, 0.3)
+    rb = C.vocab_ce(H, W, b, 0.3)
+    for x, y in zip(ra, rb):
+        np.testing.assert_array_equal(x, y)
+    assert np.all(ra[0][[2, 9, 17]] == 0) and np.all(ra[2][[2, 9, 17]] == 0)
+    keep = np.setdiff1d(np.arange(20), [2, 9, 17])
+    np.testing.assert_allclose(ra[3], C.vocab_ce(H[keep], W, t[keep], 0.3)[3], atol=1e-13)
+
+
 def test_sampled_rows_equal_the_full_evaluation():
     H, W, t = make(50, 8, 64, seed=11, ignore=0.2)
     loss, lse, dH, _ = C.vocab_ce(H, W, t, 0.1)
