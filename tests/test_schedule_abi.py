@@ -84,7 +84,28 @@ SWEEP = [s + (0, False) for s in SWEEP] + [
 ]
 
 
-@pytest.mark.parametrize("L,M,T,P,clean,W,causal", SWEEP)
+def random_sweep(n, seed):
+    """Seeded valid problems: ragged tails (P = 1), P up to 4, unit to
+    256-token blocks, any window from one token to wider than the sequence,
+    both clean-query modes, drafter shapes."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        T = int(rng.choice([32, 64, 128]))
+        M = int(rng.choice([1, 2, 4, 8, 16, 32, 64, 128, 256]))
+        P = int(rng.choice([1, 1, 2, 3, 4]))
+        B = int(rng.integers(1, 1200 // M + 1))
+        L = B * M
+        if L < 2 or L > 1200:
+            continue
+        if P > 1 and (B % (2 * P) != 0 or (L // (2 * P)) % T != 0):
+            continue
+        W = 0 if rng.random() < 0.3 else int(rng.integers(1, L + 40))
+        out.append((L, M, T, P, bool(rng.random() < 0.8), W, bool(rng.random() < 0.5)))
+    return out
+
+
+@pytest.mark.parametrize("L,M,T,P,clean,W,causal", SWEEP + random_sweep(40, 2026))
 def test_schedule_matches_oracle_tile_set_bit_exactly(L, M, T, P, clean, W, causal):
     prob = csbp.make_problem(1, L, M, 2, 1, 64, P=P, has_clean_queries=clean, tile=T,
                              window=W, clean_causal=causal)
@@ -227,24 +248,36 @@ def test_entry_points_reject_bad_arguments_without_launching():
                            bad, bad, bad, bad, 1 << 20, None) == -1
 
 
-@pytest.mark.parametrize("L,M,T,clean,W,causal,chunk", [
-    (1024, 16, 128, True, 0, False, 2), (1024, 32, 128, False, 0, False, 3),
-    (1152, 64, 128, True, 300, True, 1), (512, 16, 32, True, 0, False, 5),
-    (1040, 16, 128, True, 0, True, 4),
-])
-def test_windowed_backward_tasks_partition_the_tile_set(L, M, T, clean, W, causal, chunk):
+def random_windowed_sweep(n, seed):
+    """Random problems of `random_sweep` with at least two query tiles and a
+    backward window of 1 .. nT - 1 tiles."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for L, M, T, P, clean, W, causal in random_sweep(4 * n, seed):
+        nT = -(-L // T)
+        if nT >= 2 and len(out) < n:
+            out.append((L, M, T, P, clean, W, causal, int(rng.integers(1, nT))))
+    return out
+
+
+@pytest.mark.parametrize("L,M,T,P,clean,W,causal,chunk", [
+    (1024, 16, 128, 1, True, 0, False, 2), (1024, 32, 128, 1, False, 0, False, 3),
+    (1152, 64, 128, 1, True, 300, True, 1), (512, 16, 32, 1, True, 0, False, 5),
+    (1040, 16, 128, 1, True, 0, True, 4),
+] + random_windowed_sweep(20, 2027))
+def test_windowed_backward_tasks_partition_the_tile_set(L, M, T, P, clean, W, causal, chunk):
     """With a query-tile window smaller than the tile count, every backward
     task covers one window (counted from the last query tile), flags its
     dK/dV for fp32 accumulation, and the tasks together hold every allowed
     (query tile, key tile) pair exactly once; windows run in order, heaviest
     first within a window."""
-    prob = csbp.make_problem(1, L, M, 2, 1, 64, has_clean_queries=clean, tile=T, window=W,
-                             clean_causal=causal, bwd_chunk=chunk)
+    prob = csbp.make_problem(1, L, M, 2, 1, 64, P=P, has_clean_queries=clean, tile=T,
+                             window=W, clean_causal=causal, bwd_chunk=chunk)
     _, _, words, info = csbp.block_schedule(prob)
     h = words[:16]
     off_bt, off_bs = int(h[13]), int(h[14])
     nT = -(-L // T)
-    want = {x[:4] for x in O.tile_pairs(L, M, T, T, 1, clean, W, causal)}
+    want = {x[:4] for x in O.tile_pairs(L, M, T, T, P, clean, W, causal)}
     seen = []
     order = []
     for t in range(info.n_bwd_tasks):
