@@ -274,13 +274,18 @@ def test_lse_merge_over_random_partitions_equals_unsharded(n_parts):
     np.testing.assert_allclose(z2, z_ref, atol=1e-12)
 
 
-@pytest.mark.parametrize("P,clean", [(1, True), (2, True), (4, True), (2, False)])
-def test_sharded_forward_equals_unsharded(P, clean):
+@pytest.mark.parametrize("P,clean,W,causal", [
+    (1, True, 0, False), (2, True, 0, False), (4, True, 0, False), (2, False, 0, False),
+    # windows leave most shards empty for most rows (z = -inf parts)
+    (2, True, 5, False), (4, True, 3, True), (4, False, 7, True), (2, True, 0, True),
+])
+def test_sharded_forward_equals_unsharded(P, clean, W, causal):
     L, M, d, Hq, Hkv = 32, 2, 4, 4, 2
-    t = make(L, Hq, Hkv, d, seed=60 + P, clean=clean)
-    Oc, Ox, lse = O.bd_attention_fwd(t["qc"], t["kc"], t["vc"], t["qx"], t["kx"], t["vx"], M, 0.5)
+    t = make(L, Hq, Hkv, d, seed=60 + P + W, clean=clean)
+    Oc, Ox, lse = O.bd_attention_fwd(t["qc"], t["kc"], t["vc"], t["qx"], t["kx"], t["vx"], M, 0.5,
+                                     W, causal)
     Oc2, Ox2, lse2, (op, zp) = O.bd_attention_fwd_sharded(
-        t["qc"], t["kc"], t["vc"], t["qx"], t["kx"], t["vx"], M, 0.5, P)
+        t["qc"], t["kc"], t["vc"], t["qx"], t["kx"], t["vx"], M, 0.5, P, W, causal)
     np.testing.assert_allclose(Ox2, Ox, atol=1e-12)
     if clean:
         np.testing.assert_allclose(Oc2, Oc, atol=1e-12)
