@@ -41,7 +41,8 @@ class Problem(ctypes.Structure):
 
 class Inputs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")]
+                ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")] + [
+                    ("stride_tok", ctypes.c_int64 * 6), ("stride_batch", ctypes.c_int64 * 6)]
 
 
 class CeProblem(ctypes.Structure):
@@ -195,7 +196,9 @@ class _Checks:
         self.fn = fn
         self.seen = []
 
-    def tensor(self, name, t, dtype, shape, required=True):
+    def tensor(self, name, t, dtype, shape, required=True, strided=False):
+        """`strided`: token and batch strides are free (the library takes
+        them); heads and features must still be contiguous."""
         fn = self.fn
         if t is None:
             if required:
@@ -206,7 +209,11 @@ class _Checks:
         if shape is not None and tuple(t.shape) != tuple(shape):
             raise ValueError(f"{fn}: {name} must have shape {tuple(shape)}, "
                              f"got {tuple(t.shape)}")
-        if not t.is_contiguous():
+        if strided:
+            if t.stride(3) != 1 or (t.shape[2] > 1 and t.stride(2) != t.shape[3]):
+                raise ValueError(f"{fn}: {name} must have contiguous heads and features "
+                                 f"(strides [..., d, 1]), got {tuple(t.stride())}")
+        elif not t.is_contiguous():
             raise ValueError(f"{fn}: {name} must be contiguous")
         self.seen.append((name, t))
 
@@ -223,7 +230,8 @@ class _Checks:
                 continue
             key_side = name.startswith(("k_", "v_", "dk_", "dv_"))
             optional = not key_side and name.endswith("_clean") and not problem.has_clean_queries
-            self.tensor(name, t, torch.bfloat16, kv if key_side else q, required=not optional)
+            self.tensor(name, t, torch.bfloat16, kv if key_side else q, required=not optional,
+                        strided=name in _INPUT_NAMES)
 
     def done(self):
         for name, t in self.seen:
@@ -232,6 +240,16 @@ class _Checks:
 
 
 _INPUT_NAMES = ("q_clean", "k_clean", "v_clean", "q_corr", "k_corr", "v_corr")
+
+
+def _inputs(inputs):
+    """csbp_inputs from a dict of [batch][L][H][d] tensors: pointers, and the
+    token / batch strides of each (0 where a dimension has one entry)."""
+    ts = [inputs.get(n) for n in _INPUT_NAMES]
+    tok = [0 if t is None or t.shape[1] == 1 else t.stride(1) for t in ts]
+    bat = [0 if t is None or t.shape[0] == 1 else t.stride(0) for t in ts]
+    return Inputs(*(_ptr(t) for t in ts), (ctypes.c_int64 * 6)(*tok),
+                  (ctypes.c_int64 * 6)(*bat))
 
 
 def _stream_ptr(stream):
@@ -248,7 +266,7 @@ def attn_fwd(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse, worksp
     c.tensor("work", work_dev, torch.int32, None)
     c.tensor("workspace", workspace, torch.uint8, None)
     c.done()
-    inp = Inputs(*(_ptr(inputs.get(n)) for n in _INPUT_NAMES))
+    inp = _inputs(inputs)
     st = lib().csbp_attn_fwd(ctypes.byref(problem), ctypes.byref(inp), _ptr(work_dev),
                              ctypes.byref(info), _ptr(o_clean), _ptr(o_corr), _ptr(lse),
                              _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -273,7 +291,7 @@ def attn_bwd(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse, do_cle
     _check_bwd(c, problem, inputs, work_dev, o_clean, o_corr, lse, do_clean, do_corr, grads)
     c.tensor("workspace", workspace, torch.uint8, None)
     c.done()
-    inp = Inputs(*(_ptr(inputs.get(n)) for n in _INPUT_NAMES))
+    inp = _inputs(inputs)
     st = lib().csbp_attn_bwd(ctypes.byref(problem), ctypes.byref(inp), _ptr(work_dev),
                              ctypes.byref(info), _ptr(o_clean), _ptr(o_corr), _ptr(lse),
                              _ptr(do_clean), _ptr(do_corr), _ptr(grads.get("dq_clean")),
@@ -292,7 +310,7 @@ def attn_bwd_noalloc(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse
     c = _Checks("csbp_attn_bwd_noalloc")
     _check_bwd(c, problem, inputs, work_dev, o_clean, o_corr, lse, do_clean, do_corr, grads)
     c.done()
-    inp = Inputs(*(_ptr(inputs.get(n)) for n in _INPUT_NAMES))
+    inp = _inputs(inputs)
     st = lib().csbp_attn_bwd_noalloc(ctypes.byref(problem), ctypes.byref(inp), _ptr(work_dev),
                                      ctypes.byref(info), _ptr(o_clean), _ptr(o_corr), _ptr(lse),
                                      _ptr(do_clean), _ptr(do_corr), _ptr(grads.get("dq_clean")),

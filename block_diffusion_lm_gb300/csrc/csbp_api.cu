@@ -52,14 +52,37 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 3-D map over a bf16 [batch][L][H][d] tensor viewed as {H*d, L, batch};
 // box = 64 elements (128 B, one swizzle row) x box_rows rows x 1.
+// Element strides of one bf16 [batch][L][H][d] tensor between tokens and
+// between batch entries (heads and features are always contiguous).
+struct TokStride {
+  int64_t tok, batch;
+};
+
+TokStride contiguous_stride(int64_t H, int d, int64_t L) {
+  return {H * d, L * H * d};
+}
+
+// Strides of the i-th pointer of csbp_inputs (q_clean, k_clean, v_clean,
+// q_corr, k_corr, v_corr): the caller's, or the contiguous ones for 0.
+TokStride input_stride(const csbp_problem* p, const csbp_inputs* in, int i) {
+  const int64_t H = (i == 0 || i == 3) ? p->Hq : p->Hkv;
+  TokStride s;
+  s.tok = in->stride_tok[i] != 0 ? in->stride_tok[i] : H * p->d;
+  s.batch = (p->batch > 1 && in->stride_batch[i] != 0) ? in->stride_batch[i]
+                                                        : static_cast<int64_t>(p->L) * s.tok;
+  return s;
+}
+
+// 3-D map {H*d, L, batch} over a bf16 [batch][L][H][d] tensor with the given
+// token and batch strides; box = 64 features x box_rows tokens x 1.
 bool make_map(CUtensorMap* m, const void* base, int64_t H, int d, int64_t L, int64_t batch,
-              int box_rows = kTile) {
+              TokStride st, int box_rows = kTile) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(H * d), static_cast<cuuint64_t>(L),
                         static_cast<cuuint64_t>(batch)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(H * d * 2),
-                           static_cast<cuuint64_t>(L * H * d * 2)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(st.tok * 2),
+                           static_cast<cuuint64_t>(st.batch * 2)};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
@@ -140,8 +163,19 @@ csbp_status check_inputs(const csbp_problem* p, const csbp_inputs* in) {
     return CSBP_ERR_INVALID;
   if (p->has_clean_queries && !in->q_clean) return CSBP_ERR_INVALID;
   const void* ptrs[6] = {in->q_clean, in->k_clean, in->v_clean, in->q_corr, in->k_corr, in->v_corr};
-  for (const void* q : ptrs)
-    if (q && !aligned16(q)) return CSBP_ERR_INVALID;
+  constexpr int64_t kMaxStride = int64_t(1) << 39;  // elements: TMA strides stay below 2^40 bytes
+  for (int i = 0; i < 6; ++i) {
+    if (!ptrs[i]) continue;
+    if (!aligned16(ptrs[i])) return CSBP_ERR_INVALID;
+    if (in->stride_tok[i] < 0 || in->stride_batch[i] < 0) return CSBP_ERR_INVALID;
+    const int64_t H = (i == 0 || i == 3) ? p->Hq : p->Hkv;
+    const TokStride s = input_stride(p, in, i);
+    // 16-byte rows for TMA, and tokens / batch entries that do not overlap
+    if (s.tok < H * p->d || s.tok % 8 != 0 || s.tok >= kMaxStride) return CSBP_ERR_INVALID;
+    if (s.batch < static_cast<int64_t>(p->L) * s.tok || s.batch % 8 != 0 ||
+        s.batch >= kMaxStride)
+      return CSBP_ERR_INVALID;
+  }
   return CSBP_OK;
 }
 
@@ -282,7 +316,7 @@ extern "C" csbp_status csbp_kernel_timing_read_kind(int32_t kind, double* ms, in
   return CSBP_OK;
 }
 
-extern "C" int32_t csbp_version(void) { return 200; }  // 0.2.0: mask options, backward windows, vocabulary loss, self-test
+extern "C" int32_t csbp_version(void) { return 300; }  // 0.3.0: strided inputs
 
 extern "C" const char* csbp_status_string(csbp_status s) {
   switch (s) {
@@ -322,13 +356,14 @@ extern "C" csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inp
   const csbp_problem& p = *problem;
 
   CUtensorMap maps[6];
-  const void* qc = in->q_clean ? in->q_clean : in->q_corr;  // unused map when absent
-  if (!make_map(&maps[0], qc, p.Hq, p.d, p.L, p.batch) ||
-      !make_map(&maps[1], in->q_corr, p.Hq, p.d, p.L, p.batch) ||
-      !make_map(&maps[2], in->k_clean, p.Hkv, p.d, p.L, p.batch) ||
-      !make_map(&maps[3], in->k_corr, p.Hkv, p.d, p.L, p.batch) ||
-      !make_map(&maps[4], in->v_clean, p.Hkv, p.d, p.L, p.batch) ||
-      !make_map(&maps[5], in->v_corr, p.Hkv, p.d, p.L, p.batch))
+  const int qi = in->q_clean ? 0 : 3;  // the clean-query map is unused when absent
+  const void* qc = in->q_clean ? in->q_clean : in->q_corr;
+  if (!make_map(&maps[0], qc, p.Hq, p.d, p.L, p.batch, input_stride(problem, in, qi)) ||
+      !make_map(&maps[1], in->q_corr, p.Hq, p.d, p.L, p.batch, input_stride(problem, in, 3)) ||
+      !make_map(&maps[2], in->k_clean, p.Hkv, p.d, p.L, p.batch, input_stride(problem, in, 1)) ||
+      !make_map(&maps[3], in->k_corr, p.Hkv, p.d, p.L, p.batch, input_stride(problem, in, 4)) ||
+      !make_map(&maps[4], in->v_clean, p.Hkv, p.d, p.L, p.batch, input_stride(problem, in, 2)) ||
+      !make_map(&maps[5], in->v_corr, p.Hkv, p.d, p.L, p.batch, input_stride(problem, in, 5)))
     return CSBP_ERR_CUDA;
 
   const WorkOffsets wo = work_offsets(info);
@@ -420,20 +455,23 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
   float* dq_acc = reinterpret_cast<float*>(ws + wl.dq_acc);
 
   CUtensorMap maps[11];
+  const int qi = in->q_clean ? 0 : 3;  // the clean-query maps are unused when absent
   const void* qc = in->q_clean ? in->q_clean : in->q_corr;
   const void* dc = do_clean ? do_clean : do_corr;
+  const TokStride dos = contiguous_stride(p.Hq, p.d, p.L);
   const int qbox = bwd_query_box_rows();
   if (!make_map_dqacc(&maps[10], dq_acc, p.Hq, p.d, p.L, 2 * static_cast<int64_t>(p.batch),
                       bwd_dq_box_rows(p.d)))
     return CSBP_ERR_CUDA;
-  if (!make_map(&maps[0], qc, p.Hq, p.d, p.L, p.batch, qbox) ||
-      !make_map(&maps[1], in->q_corr, p.Hq, p.d, p.L, p.batch, qbox) ||
-      !make_map(&maps[2], in->k_clean, p.Hkv, p.d, p.L, p.batch) ||
-      !make_map(&maps[3], in->k_corr, p.Hkv, p.d, p.L, p.batch) ||
-      !make_map(&maps[4], in->v_clean, p.Hkv, p.d, p.L, p.batch) ||
-      !make_map(&maps[5], in->v_corr, p.Hkv, p.d, p.L, p.batch) ||
-      !make_map(&maps[6], dc, p.Hq, p.d, p.L, p.batch, qbox) ||
-      !make_map(&maps[7], do_corr, p.Hq, p.d, p.L, p.batch, qbox) ||
+  if (!make_map(&maps[0], qc, p.Hq, p.d, p.L, p.batch, input_stride(problem, in, qi), qbox) ||
+      !make_map(&maps[1], in->q_corr, p.Hq, p.d, p.L, p.batch, input_stride(problem, in, 3),
+                qbox) ||
+      !make_map(&maps[2], in->k_clean, p.Hkv, p.d, p.L, p.batch, input_stride(problem, in, 1)) ||
+      !make_map(&maps[3], in->k_corr, p.Hkv, p.d, p.L, p.batch, input_stride(problem, in, 4)) ||
+      !make_map(&maps[4], in->v_clean, p.Hkv, p.d, p.L, p.batch, input_stride(problem, in, 2)) ||
+      !make_map(&maps[5], in->v_corr, p.Hkv, p.d, p.L, p.batch, input_stride(problem, in, 5)) ||
+      !make_map(&maps[6], dc, p.Hq, p.d, p.L, p.batch, dos, qbox) ||
+      !make_map(&maps[7], do_corr, p.Hq, p.d, p.L, p.batch, dos, qbox) ||
       !make_map_rows_f32(&maps[8], lse, p.L, static_cast<int64_t>(p.batch) * 2 * p.Hq, qbox) ||
       !make_map_rows_f32(&maps[9], dsum, p.L, static_cast<int64_t>(p.batch) * 2 * p.Hq, qbox))
     return CSBP_ERR_CUDA;

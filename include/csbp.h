@@ -31,7 +31,8 @@
  *    passed as void*; NULL = legacy default stream).  Pointers named *_dev
  *    or documented as "device" must be device (or managed) memory of the
  *    current CUDA device.
- *  - Tensors are bf16, contiguous, layout [batch][L][heads][d] unless stated.
+ *  - Tensors are bf16, contiguous, layout [batch][L][heads][d] unless stated
+ *    (the inputs of csbp_inputs may have token and batch strides).
  *    Every device pointer must be 16-byte aligned.
  *  - Errors are reported only as csbp_status values; arguments are validated
  *    before anything is enqueued, so an error return enqueues no work.  A
@@ -94,11 +95,25 @@ typedef struct {
                            by fp32 summation order.                      */
 } csbp_problem;
 
-/* Device input tensors, bf16 [batch][L][H][d] contiguous (H = Hq for q,
- * Hkv for k/v).  q_clean may be NULL when has_clean_queries == 0.        */
+/* Device input tensors, bf16 [batch][L][H][d] (H = Hq for q, Hkv for k/v).
+ * q_clean may be NULL when has_clean_queries == 0.
+ *
+ * Within a token the H heads of d features are contiguous (head stride d).
+ * Tokens and batch entries may be strided, so q, k and v can be views into
+ * one packed projection output, [batch][L][Hq + 2 Hkv][d] for example.
+ * stride_tok[i] and stride_batch[i] are element strides for the i-th
+ * pointer above (order q_clean, k_clean, v_clean, q_corr, k_corr, v_corr):
+ *   stride_tok[i]    0 = H*d (contiguous); else >= H*d and a multiple of 8;
+ *   stride_batch[i]  0 = L*stride_tok[i]; else >= L*stride_tok[i] and a
+ *                    multiple of 8; read only when batch > 1.
+ * Both must stay below 2^39 elements, and every pointer is 16-byte aligned.
+ * A zero-initialised struct with the six pointers set is the contiguous
+ * layout.  A stride outside these rules gives CSBP_ERR_INVALID.           */
 typedef struct {
   const void *q_clean, *k_clean, *v_clean;
   const void *q_corr, *k_corr, *v_corr;
+  int64_t stride_tok[6];
+  int64_t stride_batch[6];
 } csbp_inputs;
 
 /* Summary of a work list built by csbp_block_schedule. */
@@ -272,7 +287,8 @@ const char* csbp_status_string(csbp_status status);
 
 /* Library version: major * 10000 + minor * 100 + patch.  0.2.0 (200) added
  * csbp_problem.window / clean_causal / bwd_chunk, csbp_vocab_ce (with
- * csbp_vocab_ce.h), csbp_wait_selftest and csbp_kernel_timing_read_kind. */
+ * csbp_vocab_ce.h), csbp_wait_selftest and csbp_kernel_timing_read_kind.
+ * 0.3.0 (300) added the token and batch strides of csbp_inputs. */
 int32_t csbp_version(void);
 
 #ifdef __cplusplus

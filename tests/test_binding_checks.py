@@ -34,7 +34,10 @@ def test_host_tensors_are_refused():
 @pytest.mark.parametrize("name,bad,msg", [
     ("q_corr", lambda x: x.float(), "q_corr must be torch.bfloat16"),
     ("k_clean", lambda x: x.transpose(1, 2).contiguous(), "k_clean must have shape"),
-    ("v_corr", lambda x: x.transpose(1, 2).contiguous().transpose(1, 2), "v_corr must be contiguous"),
+    ("v_corr", lambda x: x.transpose(1, 2).contiguous().transpose(1, 2),
+     "v_corr must have contiguous heads and features"),
+    ("k_corr", lambda x: x.transpose(2, 3).contiguous().transpose(2, 3),
+     "k_corr must have contiguous heads"),
     ("q_clean", lambda x: None, "q_clean is required"),
 ])
 def test_forward_inputs_are_checked(name, bad, msg):
@@ -42,6 +45,27 @@ def test_forward_inputs_are_checked(name, bad, msg):
     t[name] = bad(t[name])
     with pytest.raises(ValueError, match=msg):
         attn.forward(t)
+
+
+def test_packed_qkv_views_pass_the_layout_checks():
+    """q, k and v as views into one packed [batch][L][Hq + 2 Hkv][d] tensor
+    per copy (token stride (Hq + 2 Hkv) d) get as far as the device check;
+    outputs and dO must still be contiguous."""
+    attn, t = attn_case()
+    w = WORKLOADS["tiny"]
+    for copy in ("clean", "corr"):
+        packed = torch.cat([t[f"q_{copy}"], t[f"k_{copy}"], t[f"v_{copy}"]], dim=2)
+        t[f"q_{copy}"] = packed[:, :, :w.Hq]
+        t[f"k_{copy}"] = packed[:, :, w.Hq:w.Hq + w.Hkv]
+        t[f"v_{copy}"] = packed[:, :, w.Hq + w.Hkv:]
+        assert not t[f"k_{copy}"].is_contiguous()
+    with pytest.raises(ValueError, match="q_clean must be a CUDA tensor"):
+        attn.forward(t)
+    inp = csbp._inputs(t)
+    assert list(inp.stride_tok) == [(w.Hq + 2 * w.Hkv) * w.d] * 6
+    oc, ox, lse = attn.alloc_outputs()
+    with pytest.raises(ValueError, match="o_corr must be contiguous"):
+        attn.forward(t, out=(oc, ox.transpose(1, 2).contiguous().transpose(1, 2), lse))
 
 
 def test_forward_outputs_are_checked():

@@ -129,6 +129,54 @@ def _check_against_oracle(w, bwd_chunk=0):
                 assert rel_fro(got, want) <= TOL_REL, (k, rel_fro(got, want))
 
 
+@pytest.mark.parametrize("pad_heads,extra_tokens,clean", [(0, 0, True), (1, 3, True),
+                                                         (0, 5, False)])
+def test_packed_qkv_views_match_contiguous_inputs_and_oracle(pad_heads, extra_tokens, clean):
+    """q, k and v of each copy as views into one packed [batch][L'][Hq + 2 Hkv
+    (+ pad)][d] buffer: token stride (Hq + 2 Hkv + pad) d, batch stride
+    L' (Hq + 2 Hkv + pad) d with L' >= L.  The forward is bit-identical to the
+    contiguous inputs' (the same data through other tensor maps); the
+    gradients agree to fp32 summation order; both match the oracle."""
+    w = Workload("packed", 2, 512, 16, 4, 2, 128, has_clean_queries=clean, seed=50)
+    t = make_inputs(w, "cuda")
+    attn = csbp.BlockDiffusionAttention(w.batch, w.L, w.M, w.Hq, w.Hkv, w.d,
+                                        has_clean_queries=clean)
+    ref_o = attn.forward(t)
+    ref_g = attn.backward(t, ref_o)
+    Ht = w.Hq + 2 * w.Hkv + pad_heads
+    v = dict(t)
+    for copy in ("clean", "corr"):
+        buf = torch.zeros(w.batch, w.L + extra_tokens, Ht, w.d, dtype=torch.bfloat16,
+                          device="cuda")
+        spans = {"q": (0, w.Hq), "k": (w.Hq, w.Hq + w.Hkv), "v": (w.Hq + w.Hkv, w.Hq + 2 * w.Hkv)}
+        for x, (a, b) in spans.items():
+            if t[f"{x}_{copy}"] is None:
+                continue
+            buf[:, :w.L, a:b] = t[f"{x}_{copy}"]
+            v[f"{x}_{copy}"] = buf[:, :w.L, a:b]
+            assert not v[f"{x}_{copy}"].is_contiguous()
+    out = attn.forward(v)
+    g = attn.backward(v, out)
+    attn.check()
+    torch.cuda.synchronize()
+    for a, b in zip(out, ref_o):
+        # LSE rows of an absent clean-query stream are NaN in both
+        assert (a is None and b is None) or bool(((a == b) | (a.isnan() & b.isnan())).all())
+    for k, r in ref_g.items():
+        if r is not None:
+            assert ((g[k].double() - r.double()).norm() / r.double().norm()).item() <= 1e-5, k
+    for b in range(w.batch):
+        f = {k: (to_f64(x[b]) if x is not None else None) for k, x in t.items()}
+        _, Ox, Z = O.bd_attention_fwd(f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"],
+                                      f["k_corr"], f["v_corr"], w.M, w.scale)
+        assert np.abs(to_f64(out[1][b]) - Ox).max() <= TOL_O
+        assert np.abs(to_f64(out[2][b])[1] - Z[1]).max() <= TOL_LSE
+        G = O.bd_attention_bwd(f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"],
+                               f["k_corr"], f["v_corr"], f["do_clean"], f["do_corr"], w.M, w.scale)
+        for k in ("dq_corr", "dk_clean", "dv_clean"):
+            assert rel_fro(to_f64(g[k][b]), G[k]) <= TOL_REL, k
+
+
 def test_sharded_equals_unsharded_on_gpu():
     """Per-shard partials + LSE merge (P=4) reproduce the fused unsharded pass."""
     w = Workload("shard_vs_fused", 1, 2048, 16, 4, 2, 128, P=4, seed=30)

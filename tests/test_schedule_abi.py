@@ -248,6 +248,52 @@ def test_entry_points_reject_bad_arguments_without_launching():
                            bad, bad, bad, bad, 1 << 20, None) == -1
 
 
+def test_input_strides_are_checked_before_launching():
+    """Token and batch strides of csbp_inputs: the contiguous default (0) and
+    packed-QKV views pass (the call then stops at the too-small workspace,
+    before any CUDA call); strides that break the header's rules are refused."""
+    L = csbp.lib()
+    prob = csbp.make_problem(2, 1024, 64, 4, 2, 64)  # Hq*d = 256, Hkv*d = 128
+    info = csbp.ScheduleInfo()
+    g = ctypes.c_void_p(0x10000)
+
+    def fwd(tok, bat):
+        inp = csbp.Inputs(g, g, g, g, g, g, (ctypes.c_int64 * 6)(*tok),
+                          (ctypes.c_int64 * 6)(*bat))
+        return L.csbp_attn_fwd(ctypes.byref(prob), ctypes.byref(inp), g, ctypes.byref(info),
+                               g, g, g, g, 16, None)
+
+    def bwd(tok, bat):
+        inp = csbp.Inputs(g, g, g, g, g, g, (ctypes.c_int64 * 6)(*tok),
+                          (ctypes.c_int64 * 6)(*bat))
+        return L.csbp_attn_bwd(ctypes.byref(prob), ctypes.byref(inp), g, ctypes.byref(info),
+                               *([g] * 12), 16, None)
+
+    packed = (4 + 2 * 2) * 64  # [L][Hq + 2 Hkv][d]
+    zero = [0] * 6
+    assert fwd(zero, zero) == -3 and bwd(zero, zero) == -3
+    assert fwd([packed] * 6, [1024 * packed] * 6) == -3
+    assert bwd([packed] * 6, [1024 * packed + 64] * 6) == -3
+    assert fwd([0, 128, 128, 0, 128, 128], zero) == -3  # k/v at their own H*d
+    for tok, bat in [
+        ([248, 0, 0, 0, 0, 0], zero),              # q token stride below Hq*d
+        ([0, 0, 0, 0, 120, 0], zero),              # k token stride below Hkv*d
+        ([0, packed + 4, 0, 0, 0, 0], zero),       # not a multiple of 8 elements
+        ([0, 0, -8, 0, 0, 0], zero),               # negative
+        ([0, 0, 0, 1 << 39, 0, 0], zero),          # past the TMA stride range
+        ([packed] * 6, [1024 * packed - 8] + [0] * 5),  # batch entries overlap
+        (zero, [0, 0, 0, 0, 0, 1024 * 128 + 4]),   # batch stride not a multiple of 8
+        (zero, [0, -1024 * 128, 0, 0, 0, 0]),      # negative batch stride
+    ]:
+        assert fwd(tok, bat) == -1, (tok, bat)
+        assert bwd(tok, bat) == -1, (tok, bat)
+    # with one batch entry the batch stride is not read (a negative one is
+    # still malformed)
+    prob.batch = 1
+    assert fwd(zero, [8] * 6) == -3
+    assert fwd(zero, [-8] + [0] * 5) == -1
+
+
 def random_windowed_sweep(n, seed):
     """Random problems of `random_sweep` with at least two query tiles and a
     backward window of 1 .. nT - 1 tiles."""
