@@ -1,0 +1,73 @@
+"""The C ABI from a plain C99 program: both headers compile as strict C
+(-std=c99 -pedantic -Werror), the struct layouts the C compiler gives equal
+the Python binding's ctypes structures, and the host-only entry points give
+the same answers from C as through the binding and the oracle."""
+import ctypes
+import os
+import shutil
+import subprocess
+
+import pytest
+
+from block_diffusion_lm_gb300 import csbp
+from oracle import csbp_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PKG = os.path.join(ROOT, "block_diffusion_lm_gb300")
+
+
+@pytest.fixture(scope="module")
+def c_output(tmp_path_factory):
+    from block_diffusion_lm_gb300 import build
+    build.build()
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path_factory.mktemp("cabi") / "c_abi_check")
+    cmd = [cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+           "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "c_abi_check.c"),
+           "-L", PKG, "-lcsbp", f"-Wl,-rpath,{PKG}", "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    out = {}
+    for line in r.stdout.splitlines():
+        key, _, val = line.rpartition(" ") if line.startswith(("offset", "sizeof")) \
+            else line.partition(" ")
+        out[key] = val
+    return out
+
+
+def test_struct_layouts_match_the_binding(c_output):
+    o = c_output
+    assert int(o["sizeof csbp_problem"]) == ctypes.sizeof(csbp.Problem)
+    for f in ("scale", "window", "bwd_chunk"):
+        assert int(o[f"offset csbp_problem.{f}"]) == getattr(csbp.Problem, f).offset, f
+    assert int(o["sizeof csbp_inputs"]) == ctypes.sizeof(csbp.Inputs)
+    for f in ("v_corr", "stride_tok", "stride_batch"):
+        assert int(o[f"offset csbp_inputs.{f}"]) == getattr(csbp.Inputs, f).offset, f
+    assert int(o["sizeof csbp_schedule_info"]) == ctypes.sizeof(csbp.ScheduleInfo)
+    for f in ("tile_pairs", "bytes"):
+        assert int(o[f"offset csbp_schedule_info.{f}"]) == getattr(csbp.ScheduleInfo, f).offset
+    assert int(o["sizeof csbp_ce_problem"]) == ctypes.sizeof(csbp.CeProblem)
+    for f in ("d_model", "grad_scale"):
+        assert int(o[f"offset csbp_ce_problem.{f}"]) == getattr(csbp.CeProblem, f).offset, f
+
+
+def test_host_entry_points_agree_with_the_binding_and_the_oracle(c_output):
+    o = c_output
+    assert int(o["version"]) == csbp.lib().csbp_version()
+    prob = csbp.make_problem(1, 1024, 32, 4, 2, 128, P=2)
+    bo, co, _, info = csbp.block_schedule(prob)
+    assert int(o["tile_pairs"]) == info.tile_pairs == len(O.tile_pairs(1024, 32, 128, 128, 2))
+    assert [int(x) for x in o["owner_first_last"].split()] == [bo[0], bo[31]]
+    assert [int(x) for x in o["chunk_owner"].split()] == list(co) == list(O.chunk_owner(1024, 2))
+    assert int(o["fwd_workspace"]) == csbp.workspace_bytes(prob, 0)
+    assert int(o["bwd_workspace"]) == csbp.workspace_bytes(prob, 1)
+    assert o["status_workspace"] == csbp.lib().csbp_status_string(-3).decode()
+    assert int(o["fwd_without_inputs"]) == -1
+    assert int(o["fwd_bad_stride"]) == -1
+    ce = csbp.make_ce_problem(1000, 256, 4096, 0, True, 0.001)
+    assert int(o["ce_workspace"]) == csbp.ce_workspace_bytes(ce) > 0
+    assert int(o["ce_workspace_invalid"]) == 0
