@@ -371,11 +371,11 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
                                      (int32_t)off_bs,
                                      (int32_t)total};
   std::memcpy(w, hdr, sizeof(hdr));
-  auto emit = [&](const std::vector<Task>& tasks, int64_t off_t, int64_t off_s) {
+  auto emit = [&](const std::vector<Task>& tasks, int64_t off_task, int64_t off_seg) {
     int64_t s = 0;
     for (size_t i = 0; i < tasks.size(); ++i) {
       const Task& t = tasks[i];
-      int32_t* tw = w + off_t + (int64_t)i * kTaskWords;
+      int32_t* tw = w + off_task + (int64_t)i * kTaskWords;
       tw[0] = t.a_stream;
       tw[1] = t.a_tile;
       tw[2] = t.part;
@@ -385,7 +385,7 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
       tw[6] = t.flags;
       tw[7] = t.window;
       for (const Seg& g : t.segs) {
-        int32_t* sw = w + off_s + s * kSegWords;
+        int32_t* sw = w + off_seg + s * kSegWords;
         sw[0] = g.stream;
         sw[1] = g.begin;
         sw[2] = g.end;

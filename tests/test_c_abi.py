@@ -71,3 +71,16 @@ def test_host_entry_points_agree_with_the_binding_and_the_oracle(c_output):
     ce = csbp.make_ce_problem(1000, 256, 4096, 0, True, 0.001)
     assert int(o["ce_workspace"]) == csbp.ce_workspace_bytes(ce) > 0
     assert int(o["ce_workspace_invalid"]) == 0
+
+
+def test_schedule_builder_compiles_without_warnings():
+    """The host schedule builder is plain C++17: it compiles warning-free
+    with -Wall -Wextra -Wpedantic -Wshadow as errors."""
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    cmd = [cxx, "-std=c++17", "-Wall", "-Wextra", "-Wpedantic", "-Wshadow", "-Werror",
+           "-fsyntax-only", "-I", os.path.join(ROOT, "include"),
+           "-I", "/usr/local/cuda/include", os.path.join(PKG, "csrc", "schedule.cpp")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
