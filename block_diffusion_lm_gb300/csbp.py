@@ -213,6 +213,20 @@ class _Checks:
             if t.stride(3) != 1 or (t.shape[2] > 1 and t.stride(2) != t.shape[3]):
                 raise ValueError(f"{fn}: {name} must have contiguous heads and features "
                                  f"(strides [..., d, 1]), got {tuple(t.stride())}")
+            # a zero stride means "contiguous" to the library, so a broadcast
+            # (expanded) batch or token dimension would be misread
+            if any(t.shape[i] > 1 and t.stride(i) == 0 for i in (0, 1)):
+                raise ValueError(f"{fn}: {name} has a broadcast (stride-0) batch or token "
+                                 f"dimension; materialise it first")
+            row = t.shape[2] * t.shape[3]
+            if t.shape[1] > 1 and (t.stride(1) < row or t.stride(1) % 8):
+                raise ValueError(f"{fn}: {name} token stride {t.stride(1)} must be >= H*d = "
+                                 f"{row} and a multiple of 8")
+            if t.shape[0] > 1 and (t.stride(0) < t.shape[1] * max(t.stride(1), row)
+                                   or t.stride(0) % 8):
+                raise ValueError(f"{fn}: {name} batch entries must not interleave (batch "
+                                 f"stride >= L x token stride, a multiple of 8); make a "
+                                 f"sequence-first layout batch-first")
         elif not t.is_contiguous():
             raise ValueError(f"{fn}: {name} must be contiguous")
         self.seen.append((name, t))

@@ -2,6 +2,8 @@
 pointers): wrong dtype, wrong shape or layout, non-contiguous, or host
 memory.  Every check runs before the library is called, so these tests need
 no GPU."""
+import dataclasses
+
 import pytest
 import torch
 
@@ -66,6 +68,32 @@ def test_packed_qkv_views_pass_the_layout_checks():
     oc, ox, lse = attn.alloc_outputs()
     with pytest.raises(ValueError, match="o_corr must be contiguous"):
         attn.forward(t, out=(oc, ox.transpose(1, 2).contiguous().transpose(1, 2), lse))
+
+
+def test_broadcast_views_are_refused():
+    """A zero stride means "contiguous" to the library, so an expanded
+    (stride-0) batch or token dimension must not reach it."""
+    w = WORKLOADS["tiny"]
+    attn = csbp.BlockDiffusionAttention(2, w.L, w.M, w.Hq, w.Hkv, w.d, device="cpu")
+    t = make_inputs(dataclasses.replace(w, batch=2), "cpu")
+    t["k_clean"] = t["k_clean"][:1].expand(2, -1, -1, -1)
+    with pytest.raises(ValueError, match="k_clean has a broadcast"):
+        attn.forward(t)
+    t = make_inputs(dataclasses.replace(w, batch=2), "cpu")
+    t["v_corr"] = t["v_corr"][:, :1].expand(-1, w.L, -1, -1)
+    with pytest.raises(ValueError, match="v_corr has a broadcast"):
+        attn.forward(t)
+
+
+def test_sequence_first_layouts_are_refused_with_a_clear_message():
+    """A [L][batch][H][d] tensor viewed as [batch][L][H][d] interleaves the
+    batch entries; the library takes batch-first strides only."""
+    w = WORKLOADS["tiny"]
+    attn = csbp.BlockDiffusionAttention(2, w.L, w.M, w.Hq, w.Hkv, w.d, device="cpu")
+    t = make_inputs(dataclasses.replace(w, batch=2), "cpu")
+    t["q_corr"] = t["q_corr"].transpose(0, 1).contiguous().transpose(0, 1)
+    with pytest.raises(ValueError, match="q_corr batch entries must not interleave"):
+        attn.forward(t)
 
 
 def test_forward_outputs_are_checked():
