@@ -169,9 +169,12 @@ csbp_status check_inputs(const csbp_problem* p, const csbp_inputs* in) {
     if (!aligned16(ptrs[i])) return CSBP_ERR_INVALID;
     if (in->stride_tok[i] < 0 || in->stride_batch[i] < 0) return CSBP_ERR_INVALID;
     const int64_t H = (i == 0 || i == 3) ? p->Hq : p->Hkv;
+    // 16-byte rows for TMA; one batch entry (L tokens) below 2^39 elements,
+    // tested by division so that no product can overflow
+    const int64_t tok = in->stride_tok[i] != 0 ? in->stride_tok[i] : H * p->d;
+    if (tok < H * p->d || tok % 8 != 0 || tok > (kMaxStride - 1) / p->L) return CSBP_ERR_INVALID;
     const TokStride s = input_stride(p, in, i);
-    // 16-byte rows for TMA, and tokens / batch entries that do not overlap
-    if (s.tok < H * p->d || s.tok % 8 != 0 || s.tok >= kMaxStride) return CSBP_ERR_INVALID;
+    // batch entries that do not overlap
     if (s.batch < static_cast<int64_t>(p->L) * s.tok || s.batch % 8 != 0 ||
         s.batch >= kMaxStride)
       return CSBP_ERR_INVALID;

@@ -170,6 +170,13 @@ csbp_status validate_problem(const csbp_problem* p) {
   if (p->bwd_chunk < 0) return CSBP_ERR_INVALID;
   if (p->d != 64 && p->d != 128) return CSBP_ERR_UNSUPPORTED;
   if (p->tile_q != p->tile_kv) return CSBP_ERR_UNSUPPORTED;
+  // No tensor of the problem reaches 2^39 elements (1 TiB of bf16, beyond any
+  // one GPU), so every element and byte count below stays well inside int64.
+  // Tested by division so that no product can overflow.
+  constexpr int64_t kMaxElems = int64_t(1) << 39;
+  const int64_t rows = static_cast<int64_t>(p->batch) * p->L;  // < 2^62
+  if (rows > kMaxElems || p->Hq > kMaxElems / rows || p->d > kMaxElems / (rows * p->Hq))
+    return CSBP_ERR_UNSUPPORTED;
   if (p->P > 1) {
     const int64_t B = p->L / p->M;
     if (B % (2 * p->P) != 0) return CSBP_ERR_UNSUPPORTED;

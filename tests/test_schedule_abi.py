@@ -281,6 +281,8 @@ def test_input_strides_are_checked_before_launching():
         ([0, packed + 4, 0, 0, 0, 0], zero),       # not a multiple of 8 elements
         ([0, 0, -8, 0, 0, 0], zero),               # negative
         ([0, 0, 0, 1 << 39, 0, 0], zero),          # past the TMA stride range
+        ([0, 0, 0, 0, 1 << 62, 0], zero),          # L x stride would overflow int64
+        ([0, 0, 0, 0, 0, (1 << 39) // 1024 + 8], zero),  # one batch entry past 2^39
         ([packed] * 6, [1024 * packed - 8] + [0] * 5),  # batch entries overlap
         (zero, [0, 0, 0, 0, 0, 1024 * 128 + 4]),   # batch stride not a multiple of 8
         (zero, [0, -1024 * 128, 0, 0, 0, 0]),      # negative batch stride
@@ -292,6 +294,40 @@ def test_input_strides_are_checked_before_launching():
     prob.batch = 1
     assert fwd(zero, [8] * 6) == -3
     assert fwd(zero, [-8] + [0] * 5) == -1
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_every_workload_passes_input_validation(name):
+    """Every benchmark and test workload, with contiguous and with packed-QKV
+    strides, passes the argument checks of both entry points (the calls
+    then stop at a deliberately small workspace, before any CUDA call)."""
+    w = WORKLOADS[name]
+    L = csbp.lib()
+    prob = csbp.make_problem(w.batch, w.L, w.M, w.Hq, w.Hkv, w.d, P=w.P,
+                             has_clean_queries=w.has_clean_queries, window=w.window,
+                             clean_causal=w.clean_causal)
+    info = csbp.ScheduleInfo()
+    g = ctypes.c_void_p(0x10000)
+    packed = (w.Hq + 2 * w.Hkv) * w.d
+    for tok, bat in (([0] * 6, [0] * 6), ([packed] * 6, [w.L * packed] * 6)):
+        inp = csbp.Inputs(g, g, g, g, g, g, (ctypes.c_int64 * 6)(*tok),
+                          (ctypes.c_int64 * 6)(*bat))
+        assert L.csbp_attn_fwd(ctypes.byref(prob), ctypes.byref(inp), g, ctypes.byref(info),
+                               g, g, g, g, 16, None) == -3
+        assert L.csbp_attn_bwd(ctypes.byref(prob), ctypes.byref(inp), g, ctypes.byref(info),
+                               *([g] * 12), 16, None) == -3
+
+
+@pytest.mark.parametrize("batch,L,Hq,d", [(1, 1 << 30, 1024, 128), (1 << 20, 1 << 20, 8, 64),
+                                          ((1 << 31) - 1, (1 << 31) - 1, 8, 128)])
+def test_problems_past_2_39_elements_are_unsupported(batch, L, Hq, d):
+    """No tensor may reach 2^39 elements (1 TiB of bf16): such problems are
+    refused up front, so no element or byte count can overflow int64."""
+    prob = csbp.make_problem(batch, L, 1, Hq, Hq, d)
+    assert csbp.workspace_bytes(prob, 0) == 0 and csbp.workspace_bytes(prob, 1) == 0
+    info = csbp.ScheduleInfo()
+    assert csbp.lib().csbp_block_schedule(ctypes.byref(prob), None, None, None, 0,
+                                          ctypes.byref(info)) == -2
 
 
 def random_windowed_sweep(n, seed):
