@@ -409,7 +409,11 @@ struct CeLayout {
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 bool ce_valid(const csbp_ce_problem* p) {
+  // rows x d_model below 2^39 elements (1 TiB of bf16 h): every row, element
+  // and byte count below then stays inside int64 (tested by division)
+  constexpr int64_t kMaxElems = int64_t(1) << 39;
   if (!p || p->rows < 1 || p->d_model < 64 || p->d_model > 65536 || p->d_model % 64 != 0 ||
+      p->rows > kMaxElems / p->d_model ||
       p->vocab < 64 || p->vocab > (1 << 24) || p->vocab % 64 != 0 || p->chunk_rows < 0 ||
       p->chunk_rows % BM != 0 || (p->head_grad != 0 && p->head_grad != 1) ||
       !std::isfinite(p->grad_scale))

@@ -26,7 +26,7 @@ def test_workspace_bytes_cover_logits_g_and_partials():
 
 
 @pytest.mark.parametrize("field,value", [
-    ("rows", 0), ("d_model", 96), ("d_model", 0), ("vocab", 100), ("vocab", 1 << 25),
+    ("rows", 0), ("rows", 1 << 62), ("rows", (1 << 39) // 256 + 1), ("d_model", 96), ("d_model", 0), ("vocab", 100), ("vocab", 1 << 25),
     ("chunk_rows", 100), ("chunk_rows", -128), ("head_grad", 2), ("grad_scale", float("inf")),
 ])
 def test_invalid_problems_have_no_workspace_and_are_refused(field, value):
