@@ -568,12 +568,18 @@ extern "C" csbp_status csbp_lse_merge(int32_t n_parts, const float* const* o_par
                                       int32_t d, void* o_out, float* lse_out, void* stream) {
   if (n_parts < 1 || n_parts > kMaxParts || rows < 1 || Hq < 1 || d < 4 || d % 4 != 0)
     return CSBP_ERR_INVALID;
+  // rows x Hq x d below 2^39 elements, tested by division (no overflow)
+  constexpr int64_t kMaxElems = int64_t(1) << 39;
+  if (rows > (kMaxElems - 1) / Hq || rows * Hq > (kMaxElems - 1) / d) return CSBP_ERR_INVALID;
   if (!o_parts || !lse_parts || !o_out || !lse_out) return CSBP_ERR_INVALID;
   if (!aligned16(o_out) && (d % 8 != 0 || (reinterpret_cast<uintptr_t>(o_out) & 7u)))
     return CSBP_ERR_INVALID;
+  const auto aligned4 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 3u) == 0; };
+  if (!aligned4(lse_out)) return CSBP_ERR_INVALID;  // fp32 LSE rows
   MergeArgs a;
   for (int s = 0; s < n_parts; ++s) {
-    if (!o_parts[s] || !lse_parts[s] || !aligned16(o_parts[s])) return CSBP_ERR_INVALID;
+    if (!o_parts[s] || !lse_parts[s] || !aligned16(o_parts[s]) || !aligned4(lse_parts[s]))
+      return CSBP_ERR_INVALID;
     a.o[s] = o_parts[s];
     a.z[s] = lse_parts[s];
   }

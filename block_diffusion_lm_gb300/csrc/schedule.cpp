@@ -175,7 +175,8 @@ csbp_status validate_problem(const csbp_problem* p) {
   // Tested by division so that no product can overflow.
   constexpr int64_t kMaxElems = int64_t(1) << 39;
   const int64_t rows = static_cast<int64_t>(p->batch) * p->L;  // < 2^62
-  if (rows > kMaxElems || p->Hq > kMaxElems / rows || p->d > kMaxElems / (rows * p->Hq))
+  if (rows >= kMaxElems || p->Hq > (kMaxElems - 1) / rows ||
+      p->d > (kMaxElems - 1) / (rows * p->Hq))
     return CSBP_ERR_UNSUPPORTED;
   if (p->P > 1) {
     const int64_t B = p->L / p->M;

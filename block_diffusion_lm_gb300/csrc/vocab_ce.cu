@@ -413,7 +413,7 @@ bool ce_valid(const csbp_ce_problem* p) {
   // and byte count below then stays inside int64 (tested by division)
   constexpr int64_t kMaxElems = int64_t(1) << 39;
   if (!p || p->rows < 1 || p->d_model < 64 || p->d_model > 65536 || p->d_model % 64 != 0 ||
-      p->rows > kMaxElems / p->d_model ||
+      p->rows > (kMaxElems - 1) / p->d_model ||
       p->vocab < 64 || p->vocab > (1 << 24) || p->vocab % 64 != 0 || p->chunk_rows < 0 ||
       p->chunk_rows % BM != 0 || (p->head_grad != 0 && p->head_grad != 1) ||
       !std::isfinite(p->grad_scale))

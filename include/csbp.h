@@ -234,7 +234,9 @@ csbp_status csbp_attn_bwd_noalloc(const csbp_problem* problem, const csbp_inputs
  *  o_parts   host array of n_parts device pointers, fp32 [rows][Hq][d]
  *  lse_parts host array of n_parts device pointers, fp32 [Hq][rows]
  *  o_out     device bf16 [rows][Hq][d];  lse_out device fp32 [Hq][rows]
- * 1 <= n_parts <= 64, d % 4 == 0.                                        */
+ * 1 <= n_parts <= 64, d % 4 == 0, rows x Hq x d < 2^39.  Alignment: the
+ * o_parts 16 bytes, o_out 16 bytes (8 when d % 8 == 0), the LSE arrays 4
+ * bytes; anything else gives CSBP_ERR_INVALID before a launch.           */
 csbp_status csbp_lse_merge(int32_t n_parts, const float* const* o_parts,
                            const float* const* lse_parts, int64_t rows, int32_t Hq,
                            int32_t d, void* o_out, float* lse_out, void* stream);

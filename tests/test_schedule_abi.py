@@ -241,6 +241,15 @@ def test_entry_points_reject_bad_arguments_without_launching():
     arr = (ctypes.c_void_p * 1)(None)
     assert L.csbp_lse_merge(0, arr, arr, 16, 2, 64, None, None, None) == -1
     assert L.csbp_lse_merge(1, arr, arr, 16, 2, 64, None, None, None) == -1
+    # fp32 LSE pointers must be 4-byte aligned; sizes must stay below 2^39
+    # elements (checked without overflow)
+    g16 = ctypes.c_void_p(0x10000)
+    ok = (ctypes.c_void_p * 1)(0x10000)
+    odd = (ctypes.c_void_p * 1)(0x10002)
+    assert L.csbp_lse_merge(1, ok, odd, 16, 2, 64, g16, g16, None) == -1
+    assert L.csbp_lse_merge(1, ok, ok, 16, 2, 64, g16, ctypes.c_void_p(0x10001), None) == -1
+    assert L.csbp_lse_merge(1, ok, ok, 1 << 62, 2, 64, g16, g16, None) == -1
+    assert L.csbp_lse_merge(1, ok, ok, 1 << 30, 4, 128, g16, g16, None) == -1
     # misaligned (odd) pointers
     bad = ctypes.c_void_p(0x1001)
     inp = csbp.Inputs(bad, bad, bad, bad, bad, bad)
