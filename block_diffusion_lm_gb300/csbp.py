@@ -54,7 +54,8 @@ class CeProblem(ctypes.Structure):
 class ScheduleInfo(ctypes.Structure):
     _fields_ = [("n_fwd_tasks", ctypes.c_int32), ("n_fwd_segments", ctypes.c_int32),
                 ("n_bwd_tasks", ctypes.c_int32), ("n_bwd_segments", ctypes.c_int32),
-                ("tile_pairs", ctypes.c_int64), ("bytes", ctypes.c_int64)]
+                ("tile_pairs", ctypes.c_int64), ("bytes", ctypes.c_int64),
+                ("problem_key", ctypes.c_uint64)]
 
 
 _lib = None

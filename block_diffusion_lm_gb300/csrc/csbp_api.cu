@@ -27,6 +27,7 @@ cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, float* Dsum, fl
 cudaError_t launch_dq_convert(const float* acc, void* dq, int64_t n_elems, float scale,
                               cudaStream_t stream);
 cudaError_t launch_fill(float* x, int64_t n, float v, cudaStream_t stream);
+uint64_t schedule_key(const csbp_problem* p);
 
 namespace {
 
@@ -349,6 +350,7 @@ extern "C" csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inp
   if (problem->tile_q != kTile) return CSBP_ERR_UNSUPPORTED;
   if ((st = check_inputs(problem, in)) != CSBP_OK) return st;
   if (!work_dev || !info || !o_corr || !lse || !workspace) return CSBP_ERR_INVALID;
+  if (info->problem_key != schedule_key(problem)) return CSBP_ERR_INVALID;  // another problem's list
   if (problem->has_clean_queries && !o_clean) return CSBP_ERR_INVALID;
   if (!aligned16(work_dev) || !aligned16(o_corr) || (o_clean && !aligned16(o_clean)) ||
       !aligned16(lse) || !aligned16(workspace))
@@ -444,6 +446,7 @@ extern "C" csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inp
       !dk_corr || !dv_corr || !workspace)
     return CSBP_ERR_INVALID;
   if (hc && (!o_clean || !do_clean || !dq_clean)) return CSBP_ERR_INVALID;
+  if (info->problem_key != schedule_key(problem)) return CSBP_ERR_INVALID;  // another problem's list
   const void* all[] = {work_dev, o_corr, lse, do_corr, dq_corr, dk_clean, dv_clean, dk_corr,
                        dv_corr, workspace, o_clean, do_clean, dq_clean};
   for (const void* q : all)

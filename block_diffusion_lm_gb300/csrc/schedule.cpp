@@ -187,6 +187,22 @@ csbp_status validate_problem(const csbp_problem* p) {
   return CSBP_OK;
 }
 
+// FNV-1a over the problem fields a work list depends on (batch, heads, d and
+// the scale do not change it): lets the attention entry points refuse a list
+// built for another problem.
+uint64_t schedule_key(const csbp_problem* p) {
+  const int32_t f[9] = {p->L, p->M, p->tile_q, p->tile_kv, p->P, p->has_clean_queries,
+                        p->window, p->clean_causal, p->bwd_chunk};
+  uint64_t h = 1469598103934665603ull;
+  for (int32_t v : f) {
+    for (int b = 0; b < 4; ++b) {
+      h ^= static_cast<uint64_t>((static_cast<uint32_t>(v) >> (8 * b)) & 0xffu);
+      h *= 1099511628211ull;
+    }
+  }
+  return h;
+}
+
 int64_t bwd_chunk_tiles(const csbp_problem* p) { return p->bwd_chunk; }
 
 bool bwd_windowed(const csbp_problem* p) {
@@ -358,6 +374,7 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
   info->n_bwd_segments = (int32_t)n_bseg;
   info->tile_pairs = pairs;
   info->bytes = total * (int64_t)sizeof(int32_t);
+  info->problem_key = schedule_key(problem);
   if (!work || work_cap < info->bytes) return CSBP_ERR_CAPACITY;
 
   int32_t* w = static_cast<int32_t*>(work);

@@ -124,6 +124,11 @@ typedef struct {
   int32_t n_bwd_segments; /* query-tile ranges of the backward tasks      */
   int64_t tile_pairs;     /* (query tile, key tile) pairs with >=1 allowed entry */
   int64_t bytes;          /* size of the work list                        */
+  uint64_t problem_key;   /* opaque fingerprint of the problem fields the
+                             list depends on (L, M, tiles, P, query copies,
+                             window, clean_causal, bwd_chunk); the attention
+                             entry points refuse, with CSBP_ERR_INVALID, an
+                             info whose key does not match their problem   */
 } csbp_schedule_info;
 
 /* Work-list layout (int32 words; produced and consumed only by this library
@@ -290,7 +295,8 @@ const char* csbp_status_string(csbp_status status);
 /* Library version: major * 10000 + minor * 100 + patch.  0.2.0 (200) added
  * csbp_problem.window / clean_causal / bwd_chunk, csbp_vocab_ce (with
  * csbp_vocab_ce.h), csbp_wait_selftest and csbp_kernel_timing_read_kind.
- * 0.3.0 (300) added the token and batch strides of csbp_inputs. */
+ * 0.3.0 (300) added the token and batch strides of csbp_inputs and
+ * csbp_schedule_info.problem_key. */
 int32_t csbp_version(void);
 
 #ifdef __cplusplus

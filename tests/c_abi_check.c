@@ -42,6 +42,7 @@ int main(void) {
   printf("sizeof csbp_schedule_info %zu\n", sizeof(csbp_schedule_info));
   LAYOUT(csbp_schedule_info, tile_pairs);
   LAYOUT(csbp_schedule_info, bytes);
+  LAYOUT(csbp_schedule_info, problem_key);
   printf("sizeof csbp_ce_problem %zu\n", sizeof(csbp_ce_problem));
   LAYOUT(csbp_ce_problem, d_model);
   LAYOUT(csbp_ce_problem, grad_scale);
@@ -83,6 +84,18 @@ int main(void) {
                      (void*)(uintptr_t)0x10000, (void*)(uintptr_t)0x10000,
                      (float*)(uintptr_t)0x10000, (void*)(uintptr_t)0x10000, 1 << 30, NULL);
   printf("fwd_bad_stride %d\n", (int)st);
+  /* the list was built for L = 1024: a problem of another length refuses it */
+  in.stride_tok[1] = 0;
+  p.L = 2048;
+  st = csbp_attn_fwd(&p, &in, (const void*)(uintptr_t)0x10000, &info,
+                     (void*)(uintptr_t)0x10000, (void*)(uintptr_t)0x10000,
+                     (float*)(uintptr_t)0x10000, (void*)(uintptr_t)0x10000, 16, NULL);
+  printf("fwd_other_problem %d\n", (int)st);
+  p.L = 1024;
+  st = csbp_attn_fwd(&p, &in, (const void*)(uintptr_t)0x10000, &info,
+                     (void*)(uintptr_t)0x10000, (void*)(uintptr_t)0x10000,
+                     (float*)(uintptr_t)0x10000, (void*)(uintptr_t)0x10000, 16, NULL);
+  printf("fwd_small_workspace %d\n", (int)st);
 
   ce.rows = 1000;
   ce.d_model = 256;

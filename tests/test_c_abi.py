@@ -48,7 +48,7 @@ def test_struct_layouts_match_the_binding(c_output):
     for f in ("v_corr", "stride_tok", "stride_batch"):
         assert int(o[f"offset csbp_inputs.{f}"]) == getattr(csbp.Inputs, f).offset, f
     assert int(o["sizeof csbp_schedule_info"]) == ctypes.sizeof(csbp.ScheduleInfo)
-    for f in ("tile_pairs", "bytes"):
+    for f in ("tile_pairs", "bytes", "problem_key"):
         assert int(o[f"offset csbp_schedule_info.{f}"]) == getattr(csbp.ScheduleInfo, f).offset
     assert int(o["sizeof csbp_ce_problem"]) == ctypes.sizeof(csbp.CeProblem)
     for f in ("d_model", "grad_scale"):
@@ -68,6 +68,8 @@ def test_host_entry_points_agree_with_the_binding_and_the_oracle(c_output):
     assert o["status_workspace"] == csbp.lib().csbp_status_string(-3).decode()
     assert int(o["fwd_without_inputs"]) == -1
     assert int(o["fwd_bad_stride"]) == -1
+    assert int(o["fwd_other_problem"]) == -1
+    assert int(o["fwd_small_workspace"]) == -3
     ce = csbp.make_ce_problem(1000, 256, 4096, 0, True, 0.001)
     assert int(o["ce_workspace"]) == csbp.ce_workspace_bytes(ce) > 0
     assert int(o["ce_workspace_invalid"]) == 0

@@ -264,6 +264,8 @@ def test_input_strides_are_checked_before_launching():
     L = csbp.lib()
     prob = csbp.make_problem(2, 1024, 64, 4, 2, 64)  # Hq*d = 256, Hkv*d = 128
     info = csbp.ScheduleInfo()
+    assert L.csbp_block_schedule(ctypes.byref(prob), None, None, None, 0,
+                                 ctypes.byref(info)) == -6  # counts and key only
     g = ctypes.c_void_p(0x10000)
 
     def fwd(tok, bat):
@@ -316,6 +318,8 @@ def test_every_workload_passes_input_validation(name):
                              has_clean_queries=w.has_clean_queries, window=w.window,
                              clean_causal=w.clean_causal)
     info = csbp.ScheduleInfo()
+    assert L.csbp_block_schedule(ctypes.byref(prob), None, None, None, 0,
+                                 ctypes.byref(info)) == -6  # counts and key only
     g = ctypes.c_void_p(0x10000)
     packed = (w.Hq + 2 * w.Hkv) * w.d
     for tok, bat in (([0] * 6, [0] * 6), ([packed] * 6, [w.L * packed] * 6)):
@@ -337,6 +341,34 @@ def test_problems_past_2_39_elements_are_unsupported(batch, L, Hq, d):
     info = csbp.ScheduleInfo()
     assert csbp.lib().csbp_block_schedule(ctypes.byref(prob), None, None, None, 0,
                                           ctypes.byref(info)) == -2
+
+
+@pytest.mark.parametrize("field,value", [("L", 2048), ("M", 32), ("P", 1), ("window", 100),
+                                         ("clean_causal", 1), ("bwd_chunk", 2),
+                                         ("has_clean_queries", 0)])
+def test_a_list_built_for_another_problem_is_refused(field, value):
+    """The info of a work list carries a fingerprint of the problem fields
+    the list depends on; changing any of them makes both entry points refuse
+    the list before any CUDA call, while batch, heads and the scale do not
+    matter to it."""
+    L = csbp.lib()
+    prob = csbp.make_problem(2, 1024, 64, 4, 2, 64, P=2)
+    _, _, _, info = csbp.block_schedule(prob)
+    g = ctypes.c_void_p(0x10000)
+    inp = csbp.Inputs(g, g, g, g, g, g)
+
+    def calls(p):
+        return (L.csbp_attn_fwd(ctypes.byref(p), ctypes.byref(inp), g, ctypes.byref(info),
+                                g, g, g, g, 16, None),
+                L.csbp_attn_bwd(ctypes.byref(p), ctypes.byref(inp), g, ctypes.byref(info),
+                                *([g] * 12), 16, None))
+
+    assert calls(prob) == (-3, -3)
+    other = csbp.make_problem(2, 1024, 64, 4, 2, 64, P=2)
+    setattr(other, field, value)
+    assert calls(other) == (-1, -1)
+    same_list = csbp.make_problem(1, 1024, 64, 8, 1, 128, P=2, scale=0.3)
+    assert calls(same_list) == (-3, -3)
 
 
 def random_windowed_sweep(n, seed):
