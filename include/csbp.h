@@ -159,8 +159,9 @@ typedef struct {
  *  chunk_owner  host int32[2P] or NULL: owner shard of each clean chunk
  *  work         host buffer for the work list, or NULL to query the size
  *  work_cap     capacity of `work` in bytes
- *  info         out: counts and the required size in bytes (always filled
- *               on CSBP_OK and CSBP_ERR_CAPACITY)
+ *  info         out: counts, the required size in bytes and the problem
+ *               fingerprint (always filled on CSBP_OK and CSBP_ERR_CAPACITY);
+ *               pass it with the list to csbp_attn_fwd / csbp_attn_bwd
  * Shard r owns clean chunks r and 2P-1-r of the 2P contiguous chunks of
  * length L/(2P); a corrupted block is owned by the owner of the chunk that
  * holds its first position (so blocks b and B-1-b pair up, 0-based).
