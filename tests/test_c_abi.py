@@ -86,3 +86,15 @@ def test_schedule_builder_compiles_without_warnings():
            "-I", "/usr/local/cuda/include", os.path.join(PKG, "csrc", "schedule.cpp")]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_headers_compile_as_strict_cpp():
+    """C++ callers (framework plugins, custom ops) include the headers too."""
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    src = '#include "csbp.h"\n#include "csbp_vocab_ce.h"\nint main() { return csbp_version() > 0 ? 0 : 1; }\n'
+    r = subprocess.run([cxx, "-std=c++17", "-Wall", "-Wextra", "-Wpedantic", "-Werror",
+                        "-fsyntax-only", "-x", "c++", "-I", os.path.join(ROOT, "include"), "-"],
+                       input=src, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
