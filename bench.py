@@ -26,6 +26,7 @@ GEMM: logits, dH and, for a trained head, dW).
 from __future__ import annotations
 
 import argparse
+import atexit
 import hashlib
 import json
 import os
@@ -170,15 +171,27 @@ class ClockSampler:
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
+            return
+        # the sampler loops until told to stop: end it even if the timed
+        # region raises and stop() is never reached
+        atexit.register(self._end)
 
-    def stop(self):
-        if self.proc is None:
-            return None
+    def _end(self):
+        """Terminate the sampler (kill it if it lingers); safe to call twice."""
+        if self.proc is None or self.proc.poll() is not None:
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+            self.proc.wait(timeout=5)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self._end()
+        atexit.unregister(self._end)
         self.file.flush()
         self.file.seek(0)
         rows = [ln.strip().split(",") for ln in self.file if ln.strip()]

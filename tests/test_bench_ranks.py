@@ -48,3 +48,47 @@ def test_two_gloo_ranks_take_the_slowest_time():
 def test_single_process_values_pass_through():
     assert bench.max_over_ranks(3.5, "cpu") == 3.5
     assert bench.whole_job_tflops(1, 1e12, 1000.0) == pytest.approx(1.0)
+
+
+def _fake_smi(real_popen, line):
+    """A stand-in for `nvidia-smi -lms`: prints one CSV sample line every
+    50 ms until it is terminated."""
+    import sys
+
+    def popen(cmd, **kw):
+        code = f"import time\nwhile True:\n print({line!r}, flush=True)\n time.sleep(0.05)"
+        return real_popen([sys.executable, "-c", code], **kw)
+    return popen
+
+
+def test_clock_sampler_parses_samples_and_ends_its_child(monkeypatch):
+    import subprocess
+    import time
+    line = "0, 1980, 2070, 910.5, 0x4, Not Active, Not Active, Not Active, Active"
+    monkeypatch.setattr(bench.subprocess, "Popen", _fake_smi(subprocess.Popen, line))
+    c = bench.ClockSampler(0)
+    c.start()
+    time.sleep(0.3)
+    got = c.stop()
+    assert c.proc.poll() is not None
+    assert got["sm_mhz"] == 1980.0 and got["sm_max_mhz"] == 2070.0
+    assert got["samples"] >= 1 and got["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_child_ends_even_without_stop(monkeypatch):
+    """The sampler registers its own end at interpreter exit, so a timed
+    region that raises leaves no nvidia-smi loop behind; ending twice is
+    harmless."""
+    import subprocess
+    import time
+    monkeypatch.setattr(bench.subprocess, "Popen",
+                        _fake_smi(subprocess.Popen, "0, 1, 2, 3, 0x0, a, b, c, d"))
+    c = bench.ClockSampler(0)
+    c.start()
+    time.sleep(0.1)
+    assert c.proc.poll() is None
+    c._end()          # what the exit hook runs
+    c._end()
+    assert c.proc.poll() is not None
+    got = c.stop()    # stop after the end still reads what was sampled
+    assert got["sm_mhz"] == 1.0 and got["reasons"] == []
