@@ -127,13 +127,15 @@ __global__ void __launch_bounds__(256) fill_kernel(float* x, int64_t n, float v)
 }
 
 int grid_for(int64_t work_items) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
+  // SM count of the device in use at the first call (a thread-safe static);
+  // 152, the GB300's count, if the query fails
+  static const int sms = [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 152;
+    return n;
+  }();
   const int64_t blocks = (work_items + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 resident 256-thread CTAs per SM
   return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
