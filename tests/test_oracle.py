@@ -40,15 +40,21 @@ def test_mask_matches_hand_written_fixture():
 
 def test_forward_matches_hand_worked_fixture():
     """O and LSE of all four rows of a two-block, one-token-per-block problem
-    whose scores are logs of small integers, worked out by hand."""
+    whose scores are logs of small integers, and every gradient for dO = 1,
+    worked out by hand."""
     rows = [[float(x) for x in r.split()] for r in read_golden("attention_L2_M1.txt")]
-    inp, want = np.array(rows[:2]), np.array(rows[2:])
+    inp, want, grads = np.array(rows[:2]), np.array(rows[2:4]), np.array(rows[4:6])
     qc, kc, vc, qx, kx, vx = (inp[:, c].reshape(2, 1, 1) for c in range(6))
     Oc, Ox, lse = O.bd_attention_fwd(qc, kc, vc, qx, kx, vx, M=1, scale=1.0)
     np.testing.assert_allclose(Oc[:, 0, 0], want[:, 0], atol=1e-14)
     np.testing.assert_allclose(lse[CLEAN, 0], want[:, 1], atol=1e-14)
     np.testing.assert_allclose(Ox[:, 0, 0], want[:, 2], atol=1e-14)
     np.testing.assert_allclose(lse[CORR, 0], want[:, 3], atol=1e-14)
+    ones = np.ones((2, 1, 1))
+    G = O.bd_attention_bwd(qc, kc, vc, qx, kx, vx, ones, ones, M=1, scale=1.0)
+    for c, name in enumerate(("dq_clean", "dk_clean", "dv_clean", "dq_corr", "dk_corr",
+                              "dv_corr")):
+        np.testing.assert_allclose(G[name][:, 0, 0], grads[:, c], atol=1e-14, err_msg=name)
 
 
 def test_mask_agrees_with_scalar_predicate_and_rows():
