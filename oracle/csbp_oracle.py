@@ -5,7 +5,9 @@ execute this module; only the test suite, the smoke check and the CPU-baseline
 leg of the benchmark use it.  It shares no code with the CUDA library.
 
 Every function is the plain definition written out in float64 NumPy, in the
-order and notation of the pages it follows:
+order and notation of the pages it follows (the row- and key-sampled
+evaluators for long sequences use float64 PyTorch CPU ops, which run their
+element-wise passes on every host core):
 
 * [Blog] "CSBP 完全拆解：块并行如何让长上下文扩散语言模型少传无效 KV"
   (pinghaoyang.com.cn), sections
@@ -459,33 +461,112 @@ def tile_pairs(L, M, Tq, Tkv, P=1, has_clean_queries=True, window=0, clean_causa
 
 # --------------------------------------------------------------------------
 # Row / key sampled evaluation for long sequences
+#
+# The same definitions as `masked_attention` / `masked_attention_bwd`, for a
+# subset of rows or keys of sequences too long for the explicit 2L x 2L mask.
+# They run in float64 PyTorch CPU ops, whose element-wise passes use every
+# host core (the NumPy ones run on one), on chunks of rows at a time.
 # --------------------------------------------------------------------------
+def mask_rows(rows, L: int, M: int, window: int = 0, clean_causal: bool = False) -> np.ndarray:
+    """Rows [(q_stream, i)] of `bd_mask` as one bool array [len(rows), 2L]
+    (the rules of `mask_row`, evaluated for all the rows at once)."""
+    qs = np.array([r[0] for r in rows], dtype=np.int64)[:, None]
+    i = np.array([r[1] for r in rows], dtype=np.int64)[:, None]
+    pos = np.arange(L, dtype=np.int64)[None, :]
+    b, bi = pos // M, i // M
+    clean_rule = (pos <= i) if clean_causal else (b <= bi)
+    left = np.where(qs == CLEAN, clean_rule, b < bi)           # clean keys
+    right = (qs == CORR) & (b == bi)                           # corrupted keys
+    if window > 0:
+        near = (i - pos) < window
+        left &= near
+        right &= near
+    return np.concatenate([left, right], axis=1)
+
+
 def _kv_of_head(kc, kx, vc, vx, g):
+    """[2L, d] float64 K and V of KV head g, clean keys first."""
     K = np.concatenate([np.asarray(kc[:, g], np.float64), np.asarray(kx[:, g], np.float64)], 0)
     V = np.concatenate([np.asarray(vc[:, g], np.float64), np.asarray(vx[:, g], np.float64)], 0)
     return K, V
 
 
 def _gather_rows(qc, qx, doc, dox, rows, h):
-    """Query and dO vectors of rows [(q_stream, i)] for query head h."""
-    q = np.stack([np.asarray((qc if qs == CLEAN else qx)[i, h], np.float64) for qs, i in rows])
-    do = np.stack([np.asarray((doc if qs == CLEAN else dox)[i, h], np.float64) for qs, i in rows])
+    """Query and dO vectors [len(rows), d] of rows [(q_stream, i)] for query
+    head h (one indexing per copy)."""
+    n = len(rows)
+    d = np.shape(qx)[2]
+    q = np.empty((n, d))
+    do = np.empty((n, d))
+    for stream, (qsrc, dsrc) in ((CLEAN, (qc, doc)), (CORR, (qx, dox))):
+        at = [n_ for n_, (qs, _) in enumerate(rows) if qs == stream]
+        if at:
+            idx = np.array([rows[n_][1] for n_ in at], dtype=np.int64)
+            q[at] = np.asarray(qsrc[idx, h], np.float64)
+            do[at] = np.asarray(dsrc[idx, h], np.float64)
     return q, do
 
 
+def _t64(x):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64))
+
+
+def _tbool(x):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=bool))
+
+
+def _softmax_rows_t(q, K, V, allow, scale, want_p=True):
+    """`masked_attention` in float64 torch for rows with at least one allowed
+    key: q [n,d], K/V [m,d], allow [n,m] bool -> (P [n,m] or None, O [n,d],
+    lse [n])."""
+    s = (q @ K.T) * scale
+    s.masked_fill_(~allow, float("-inf"))
+    m = s.amax(dim=1, keepdim=True)
+    e = s.sub_(m).exp_()               # exp(-inf) = 0 off the mask
+    l = e.sum(dim=1, keepdim=True)
+    o = (e @ V) / l
+    return (e.div_(l) if want_p else None), o, (m + l.log()).squeeze(1)
+
+
+def _default_chunk(L):
+    """Rows per chunk so that a chunk's [rows, 2L] float64 arrays stay
+    within about 1 GB each."""
+    return int(max(8, min(1024, (1 << 27) // (2 * L))))
+
+
+def _chunk_keys(allow, K, V, L):
+    """The keys a chunk of mask rows may read: in each copy, the range from
+    its first to its last allowed key (keys inside the range that no row
+    reads stay masked).  Returns (K_u, V_u, allow_u) as torch tensors."""
+    import torch
+    parts = []
+    for c in (0, 1):
+        hit = np.flatnonzero(allow[:, c * L:(c + 1) * L].any(axis=0))
+        if hit.size:
+            parts.append((c * L + int(hit[0]), c * L + int(hit[-1]) + 1))
+    Ku = torch.cat([K[a:b] for a, b in parts])
+    Vu = torch.cat([V[a:b] for a, b in parts])
+    au = np.concatenate([allow[:, a:b] for a, b in parts], axis=1)
+    return Ku, Vu, _tbool(au)
+
+
 def sampled_rows(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples, window=0,
-                 clean_causal=False):
+                 clean_causal=False, chunk_rows=None):
     """Exact O, lse, D and dQ for sampled query rows.
 
     samples: iterable of (q_stream, i, h).  Each row depends only on itself,
-    the full K/V of its KV head and dO_i, so the sampled rows of one head go
-    through `masked_attention` / `masked_attention_bwd` together with their
-    own mask rows.  Returns dict keyed by the sample tuple ->
-    (o [d], lse, D, dq [d]).
+    the full K/V of its KV head and dO_i: P_i = softmax over its allowed keys,
+    O_i = P_i V, D_i = dO_i . O_i, dS_ij = P_ij (dO_i . v_j - D_i),
+    dQ_i = scale sum_j dS_ij k_j.  Rows of one head go through in chunks
+    against the keys some row of the chunk may read.  Returns dict keyed by
+    the sample tuple -> (o [d], lse, D, dq [d]).
     """
     L, Hkv, d = np.shape(kc)
     Hq = np.shape(qx)[1]
     G = Hq // Hkv
+    chunk_rows = chunk_rows or _default_chunk(L)
     by_head = {}
     for (qs, i, h) in samples:
         by_head.setdefault(h, []).append((qs, i))
@@ -494,15 +575,20 @@ def sampled_rows(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples, window=0,
         heads = [h for h in range(g * G, (g + 1) * G) if h in by_head]
         if not heads:
             continue
-        K, V = _kv_of_head(kc, kx, vc, vx, g)
+        K, V = (_t64(x) for x in _kv_of_head(kc, kx, vc, vx, g))
         for h in heads:
-            rows = by_head[h]
-            q, do = _gather_rows(qc, qx, doc, dox, rows, h)
-            allow = np.stack([mask_row(qs, i, L, M, window, clean_causal) for qs, i in rows])
-            o, z = masked_attention(q, K, V, allow, scale)
-            dq, _, _, D = masked_attention_bwd(q, K, V, allow, scale, do)
-            for r, (qs, i) in enumerate(rows):
-                out[(qs, i, h)] = (o[r], float(z[r]), float(D[r]), dq[r])
+            rows_h = by_head[h]
+            for c0 in range(0, len(rows_h), chunk_rows):
+                rows = rows_h[c0:c0 + chunk_rows]
+                allow = mask_rows(rows, L, M, window, clean_causal)
+                Ku, Vu, au = _chunk_keys(allow, K, V, L)
+                q, do = (_t64(x) for x in _gather_rows(qc, qx, doc, dox, rows, h))
+                p, o, lse = _softmax_rows_t(q, Ku, Vu, au, scale)
+                D = (do * o).sum(dim=1)
+                ds = p * (do @ Vu.T - D[:, None])
+                dq = scale * (ds @ Ku)
+                for r, (qs, i) in enumerate(rows):
+                    out[(qs, i, h)] = (o[r].numpy(), float(lse[r]), float(D[r]), dq[r].numpy())
         del K, V
     return out
 
@@ -523,20 +609,26 @@ def readers_of_key(k_stream, j, L, M, has_clean_queries=True, window=0, clean_ca
 
 
 def sampled_keys(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples, window=0,
-                 clean_causal=False):
+                 clean_causal=False, chunk_rows=None):
     """Exact dK, dV for sampled keys (k_stream, j, g).
 
-    dK_j and dV_j sum over every query row that reads key j, over the G query
-    heads of KV head g.  The union of the sampled keys' readers goes through
-    `masked_attention_bwd` with each row's full mask (so every reader's P and
-    dS come from its own complete softmax); the sampled columns of its dK/dV
-    are then exact, because no other row reads those keys.  Keys with many
-    readers (early clean keys) are expensive; sample late or corrupted keys.
+    dK_j = scale sum_i dS_ij q_i and dV_j = sum_i P_ij dO_i, summed over every
+    query row i that reads key j and over the G query heads of KV head g, with
+    P_ij = exp(S_ij - lse_i), dP_ij = dO_i . v_j, D_i = dO_i . O_i (the same
+    sum_j P_ij dP_ij as in `masked_attention_bwd`, since O_i = sum_j P_ij v_j)
+    and dS_ij = P_ij (dP_ij - D_i).  Each reader's lse_i and O_i come from its
+    own complete masked softmax, so the union of the sampled keys' readers
+    goes through in chunks of `chunk_rows` rows, each against the keys that
+    some row of the chunk may read (the other columns of its mask rows are
+    all False).  The cost is that of the readers' full rows: an early clean
+    key is read by almost every row of the sequence.
     """
+    import torch
     L, Hkv, d = np.shape(kc)
     Hq = np.shape(qx)[1]
     G = Hq // Hkv
     has_clean = qc is not None
+    chunk_rows = chunk_rows or _default_chunk(L)
     by_g = {}
     for (ks, j, g) in samples:
         by_g.setdefault(g, []).append((ks, j))
@@ -544,19 +636,27 @@ def sampled_keys(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples, window=0,
     for g, keys in by_g.items():
         readers = sorted({r for ks, j in keys
                           for r in readers_of_key(ks, j, L, M, has_clean, window, clean_causal)})
-        K, V = _kv_of_head(kc, kx, vc, vx, g)
-        dk = np.zeros((len(keys), d))
-        dv = np.zeros((len(keys), d))
-        cols = [ks * L + j for ks, j in keys]
-        if readers:
-            allow = np.stack([mask_row(qs, i, L, M, window, clean_causal) for qs, i in readers])
+        K, V = (_t64(x) for x in _kv_of_head(kc, kx, vc, vx, g))
+        cols = np.array([ks * L + j for ks, j in keys], dtype=np.int64)
+        Kc, Vc = K[cols], V[cols]
+        dk = torch.zeros(len(keys), d, dtype=torch.float64)
+        dv = torch.zeros(len(keys), d, dtype=torch.float64)
+        for c0 in range(0, len(readers), chunk_rows):
+            rows = readers[c0:c0 + chunk_rows]
+            allow = mask_rows(rows, L, M, window, clean_causal)
+            Ku, Vu, au = _chunk_keys(allow, K, V, L)
+            ac = _tbool(allow[:, cols])
             for h in range(g * G, (g + 1) * G):
-                q, do = _gather_rows(qc, qx, doc, dox, readers, h)
-                _, dk_all, dv_all, _ = masked_attention_bwd(q, K, V, allow, scale, do)
-                dk += dk_all[cols]
-                dv += dv_all[cols]
+                q, do = (_t64(x) for x in _gather_rows(qc, qx, doc, dox, rows, h))
+                _, o, lse = _softmax_rows_t(q, Ku, Vu, au, scale, want_p=False)
+                D = (do * o).sum(dim=1)
+                p = torch.where(ac, ((q @ Kc.T) * scale - lse[:, None]).exp(),
+                                torch.zeros((), dtype=torch.float64))
+                ds = p * (do @ Vc.T - D[:, None])
+                dk += scale * (ds.T @ q)
+                dv += p.T @ do
         for n, (ks, j) in enumerate(keys):
-            out[(ks, j, g)] = (dk[n], dv[n])
+            out[(ks, j, g)] = (dk[n].numpy(), dv[n].numpy())
         del K, V
     return out
 

@@ -384,21 +384,50 @@ def test_sampled_rows_and_keys_agree_with_full_oracle():
     Oc, Ox, lse = O.bd_attention_fwd(t["qc"], t["kc"], t["vc"], t["qx"], t["kx"], t["vx"], M, 0.5)
     g = O.bd_attention_bwd(t["qc"], t["kc"], t["vc"], t["qx"], t["kx"], t["vx"],
                            t["doc"], t["dox"], M, 0.5)
-    samples = [(CLEAN, 0, 0), (CLEAN, 31, 3), (CORR, 5, 1), (CORR, 30, 2), (CORR, 0, 0)]
-    r = O.sampled_rows(t["qc"], t["kc"], t["vc"], t["qx"], t["kx"], t["vx"],
-                       t["doc"], t["dox"], M, 0.5, samples)
-    for (qs, i, h), (o, z, D, dq) in r.items():
-        np.testing.assert_allclose(o, (Oc if qs == CLEAN else Ox)[i, h], atol=1e-13)
-        assert abs(z - lse[qs, h, i]) < 1e-13
-        assert abs(D - g["D"][qs, h, i]) < 1e-13
-        np.testing.assert_allclose(dq, g["dq_clean" if qs == CLEAN else "dq_corr"][i, h], atol=1e-13)
+    samples = [(CLEAN, 0, 0), (CLEAN, 31, 3), (CORR, 5, 1), (CORR, 30, 2), (CORR, 0, 0),
+               (CLEAN, 17, 0), (CORR, 12, 0), (CLEAN, 3, 0)]
+    for chunk in (None, 1, 2):
+        r = O.sampled_rows(t["qc"], t["kc"], t["vc"], t["qx"], t["kx"], t["vx"],
+                           t["doc"], t["dox"], M, 0.5, samples, chunk_rows=chunk)
+        assert len(r) == len(samples)
+        for (qs, i, h), (o, z, D, dq) in r.items():
+            np.testing.assert_allclose(o, (Oc if qs == CLEAN else Ox)[i, h], atol=1e-13)
+            assert abs(z - lse[qs, h, i]) < 1e-13
+            assert abs(D - g["D"][qs, h, i]) < 1e-13
+            np.testing.assert_allclose(dq, g["dq_clean" if qs == CLEAN else "dq_corr"][i, h],
+                                       atol=1e-13)
     ks = [(CLEAN, 0, 0), (CLEAN, 29, 1), (CORR, 7, 1), (CORR, 16, 0)]
-    r = O.sampled_keys(t["qc"], t["kc"], t["vc"], t["qx"], t["kx"], t["vx"],
-                       t["doc"], t["dox"], M, 0.5, ks)
+    # one chunk of readers, and chunks of 1, 3 and 7 rows (ragged last chunk)
+    for chunk in (None, 1, 3, 7):
+        r = O.sampled_keys(t["qc"], t["kc"], t["vc"], t["qx"], t["kx"], t["vx"],
+                           t["doc"], t["dox"], M, 0.5, ks, chunk_rows=chunk)
+        for (st, j, kvh), (dk, dv) in r.items():
+            sfx = "clean" if st == CLEAN else "corr"
+            np.testing.assert_allclose(dk, g["dk_" + sfx][j, kvh], atol=1e-12)
+            np.testing.assert_allclose(dv, g["dv_" + sfx][j, kvh], atol=1e-12)
+    # drafter shape: no clean queries read the clean keys
+    g2 = O.bd_attention_bwd(None, t["kc"], t["vc"], t["qx"], t["kx"], t["vx"],
+                            None, t["dox"], M, 0.5)
+    r = O.sampled_keys(None, t["kc"], t["vc"], t["qx"], t["kx"], t["vx"], None, t["dox"], M,
+                       0.5, ks, chunk_rows=5)
     for (st, j, kvh), (dk, dv) in r.items():
         sfx = "clean" if st == CLEAN else "corr"
-        np.testing.assert_allclose(dk, g["dk_" + sfx][j, kvh], atol=1e-12)
-        np.testing.assert_allclose(dv, g["dv_" + sfx][j, kvh], atol=1e-12)
+        np.testing.assert_allclose(dk, g2["dk_" + sfx][j, kvh], atol=1e-12)
+        np.testing.assert_allclose(dv, g2["dv_" + sfx][j, kvh], atol=1e-12)
+
+
+def test_mask_rows_equal_the_rows_of_the_mask():
+    """The vectorised row mask of the sampled evaluators equals `mask_row`
+    (and so `bd_mask`) row by row, for every option."""
+    rng = np.random.default_rng(71)
+    for L, M, W, causal in [(48, 4, 0, False), (48, 8, 0, True), (64, 4, 9, False),
+                            (64, 16, 23, True), (30, 1, 5, False)]:
+        rows = [(int(rng.integers(0, 2)), int(rng.integers(0, L))) for _ in range(40)]
+        got = O.mask_rows(rows, L, M, W, causal)
+        want = np.stack([O.mask_row(qs, i, L, M, W, causal) for qs, i in rows])
+        assert np.array_equal(got, want)
+        A = O.bd_mask(L, M, W, causal)
+        assert np.array_equal(got, np.stack([A[qs * L + i] for qs, i in rows]))
 
 
 # ------------------------------------------------------- planted mistakes

@@ -172,7 +172,7 @@ def test_windowed_sampled_rows_and_keys_agree_with_full_oracle():
         np.testing.assert_allclose(dq, g["dq_clean" if qs == 0 else "dq_corr"][i, h], atol=1e-12)
     keys = [(0, 30, 0), (1, 5, 0), (0, 2, 0)]
     got = O.sampled_keys(t["qc"], t["kc"], t["vc"], t["qx"], t["kx"], t["vx"], t["doc"],
-                         t["dox"], M, 0.5, keys, W, True)
+                         t["dox"], M, 0.5, keys, W, True, chunk_rows=4)
     for (ks, j, gg), (dk, dv) in got.items():
         np.testing.assert_allclose(dk, g["dk_clean" if ks == 0 else "dk_corr"][j, gg], atol=1e-12)
         np.testing.assert_allclose(dv, g["dv_clean" if ks == 0 else "dv_corr"][j, gg], atol=1e-12)
