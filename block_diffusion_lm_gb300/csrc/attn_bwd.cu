@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include "csbp_internal.h"
+#include "device_once.h"
 #include "ptx_sm100.cuh"
 #include "work_checks.cuh"
 
@@ -672,13 +673,17 @@ template <int D>
 static cudaError_t launch_bwd_d(const CUtensorMap* maps, const BwdParams& p, int n_tasks,
                                 cudaStream_t stream) {
   using Lay = BwdLayout<D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Lay::kDynSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // the shared-memory limit is a per-device attribute: set it once on each
+  static PerDeviceOnce configured;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (!configured.run(dev, [&](int) {
+        e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Lay::kDynSmem);
+        return e == cudaSuccess;
+      }))
+    return e != cudaSuccess ? e : cudaErrorInvalidDevice;
   const int64_t grid = static_cast<int64_t>(n_tasks) * p.Hkv * p.batch;
   if (grid <= 0) return cudaSuccess;
   bwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, Lay::kDynSmem, stream>>>(

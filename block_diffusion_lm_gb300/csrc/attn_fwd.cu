@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include "csbp_internal.h"
+#include "device_once.h"
 #include "ptx_sm100.cuh"
 #include "work_checks.cuh"
 
@@ -491,21 +492,27 @@ template <int D>
 static cudaError_t launch_fwd_d(const CUtensorMap* maps, const FwdParams& p, int n_tasks,
                                 cudaStream_t stream) {
   using Lay = FwdLayout<D>;
-  static bool configured = false;
-  static int launch_regs = 0;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Lay::kDynSmem);
-    if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, fwd_kernel<D>);
-    if (e != cudaSuccess) return e;
-    launch_regs = fa.numRegs;
-    configured = true;
-  }
+  // the shared-memory limit is a per-device attribute: set it once on each
+  // device, and read the kernel's register count there
+  static PerDeviceOnce configured;
+  static int launch_regs[PerDeviceOnce::kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (!configured.run(dev, [&](int device) {
+        e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Lay::kDynSmem);
+        if (e != cudaSuccess) return false;
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, fwd_kernel<D>);
+        if (e != cudaSuccess) return false;
+        launch_regs[device] = fa.numRegs;
+        return true;
+      }))
+    return e != cudaSuccess ? e : cudaErrorInvalidDevice;
   // setmaxnreg.inc would wait forever if the budgets exceeded the launch
   // allocation: refuse to launch instead
-  if (launch_regs * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+  if (launch_regs[dev] * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
   const int64_t grid = static_cast<int64_t>((n_tasks + 1) / 2) * p.Hq * p.batch;
   if (grid <= 0) return cudaSuccess;
   fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, Lay::kDynSmem, stream>>>(

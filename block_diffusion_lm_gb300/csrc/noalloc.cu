@@ -9,6 +9,7 @@
 // fixed-size array in device global memory, reserved when the library's
 // device code is loaded and held by every GPU that loads it until the
 // process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -25,23 +26,53 @@ static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_dev[kMaxDevices] = {};
+struct ScratchAddr {
+  CUcontext ctx;  // context the address was looked up in
+  void* addr;
+};
+ScratchAddr g_scratch_dev[kMaxDevices] = {};
+
+// The CUDA context current on this thread (the device's primary context for
+// callers of the runtime API), through the runtime's driver entry point so
+// that the library needs no link against the driver library.
+CUcontext current_context() {
+  using Fn = CUresult (*)(CUcontext*);
+  static Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(f);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
 
 // Device address of g_bwd_scratch on the current device.  In host code the
-// array's name only stands in for the symbol; the address is looked up once
-// per device (with that device current) and cached.
+// array's name only stands in for the symbol; the address is looked up (with
+// that device current) the first time a context uses it, and cached for that
+// device and context.  A call from another context of the same device (a
+// driver-API context made current) looks it up again.
 csbp_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CSBP_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return CSBP_ERR_UNSUPPORTED;
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_dev[dev]) {
+  ScratchAddr& e = g_scratch_dev[dev];
+  if (!e.addr || e.ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr)
       return CSBP_ERR_CUDA;
-    g_scratch_dev[dev] = p;
+    // the runtime makes a context current if none was: key on that one
+    e.ctx = ctx ? ctx : current_context();
+    e.addr = p;
   }
-  *out = g_scratch_dev[dev];
+  *out = e.addr;
   return CSBP_OK;
 }
 
@@ -67,4 +98,11 @@ extern "C" csbp_status csbp_attn_bwd_noalloc(
   return csbp_attn_bwd(problem, in, work_dev, info, o_clean, o_corr, lse, do_clean, do_corr,
                        dq_clean, dq_corr, dk_clean, dv_clean, dk_corr, dv_corr, scratch,
                        kScratchBytes, stream);
+}
+
+extern "C" csbp_status csbp_attn_bwd_noalloc_status(void* stream) {
+  void* scratch = nullptr;
+  const csbp_status sa = scratch_address(&scratch);
+  if (sa != CSBP_OK) return sa;
+  return csbp_check_status(scratch, stream);  // the status word opens the scratch
 }

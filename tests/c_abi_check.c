@@ -35,6 +35,8 @@ int main(void) {
   LAYOUT(csbp_problem, scale);
   LAYOUT(csbp_problem, window);
   LAYOUT(csbp_problem, bwd_chunk);
+  LAYOUT(csbp_problem, per_rank);
+  LAYOUT(csbp_problem, rank);
   printf("sizeof csbp_inputs %zu\n", sizeof(csbp_inputs));
   LAYOUT(csbp_inputs, v_corr);
   LAYOUT(csbp_inputs, stride_tok);

@@ -42,7 +42,7 @@ def c_output(tmp_path_factory):
 def test_struct_layouts_match_the_binding(c_output):
     o = c_output
     assert int(o["sizeof csbp_problem"]) == ctypes.sizeof(csbp.Problem)
-    for f in ("scale", "window", "bwd_chunk"):
+    for f in ("scale", "window", "bwd_chunk", "per_rank", "rank"):
         assert int(o[f"offset csbp_problem.{f}"]) == getattr(csbp.Problem, f).offset, f
     assert int(o["sizeof csbp_inputs"]) == ctypes.sizeof(csbp.Inputs)
     for f in ("v_corr", "stride_tok", "stride_batch"):
@@ -98,3 +98,25 @@ def test_headers_compile_as_strict_cpp():
                         "-fsyntax-only", "-x", "c++", "-I", os.path.join(ROOT, "include"), "-"],
                        input=src, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_kernel_setup_runs_once_per_device(tmp_path):
+    """The launchers set a kernel's shared-memory limit once per device
+    ordinal (csrc/device_once.h): a second device gets its own set-up, a
+    failed set-up is retried, and racing threads run it once."""
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    exe = str(tmp_path / "device_once_check")
+    cmd = [cxx, "-std=c++17", "-Wall", "-Wextra", "-Werror", "-pthread",
+           "-I", os.path.join(PKG, "csrc"), os.path.join(ROOT, "tests", "device_once_check.cpp"),
+           "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    lines = r.stdout.splitlines()
+    assert lines[0] == "first 1 1 1 calls 1 1 done2 0"
+    assert lines[1] == "retry 0 1 1 tries 2"
+    assert lines[2] == "outside 0 0 runs 0"
+    assert lines[3] == "race calls 1 ok 16"
