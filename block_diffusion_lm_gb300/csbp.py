@@ -36,7 +36,8 @@ class Problem(ctypes.Structure):
                 ("P", ctypes.c_int32), ("tile_q", ctypes.c_int32), ("tile_kv", ctypes.c_int32),
                 ("has_clean_queries", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("window", ctypes.c_int32), ("clean_causal", ctypes.c_int32),
-                ("bwd_chunk", ctypes.c_int32)]
+                ("bwd_chunk", ctypes.c_int32), ("per_rank", ctypes.c_int32),
+                ("rank", ctypes.c_int32)]
 
 
 class Inputs(ctypes.Structure):
@@ -90,6 +91,8 @@ def lib():
         L.csbp_attn_bwd_noalloc.argtypes = [P(Problem), P(Inputs), vp, P(ScheduleInfo), vp, vp,
                                             vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.csbp_attn_bwd_noalloc.restype = ctypes.c_int
+        L.csbp_attn_bwd_noalloc_status.argtypes = [vp]
+        L.csbp_attn_bwd_noalloc_status.restype = ctypes.c_int
         L.csbp_lse_merge.argtypes = [i32, P(vp), P(vp), i64, i32, i32, vp, vp, vp]
         L.csbp_check_status.argtypes = [vp, vp]
         L.csbp_status_string.argtypes = [ctypes.c_int]
@@ -128,10 +131,12 @@ def _check(fn, status):
 
 
 def make_problem(batch, L, M, Hq, Hkv, d, P=1, has_clean_queries=True, scale=None,
-                 tile=128, window=0, clean_causal=False, bwd_chunk=0) -> Problem:
+                 tile=128, window=0, clean_causal=False, bwd_chunk=0, rank=None) -> Problem:
+    """rank=None: every query row; rank=r: only the rows CSBP rank r of P owns."""
     return Problem(batch, L, M, Hq, Hkv, d, P, tile, tile, 1 if has_clean_queries else 0,
                    float(scale if scale is not None else d ** -0.5), int(window),
-                   1 if clean_causal else 0, int(bwd_chunk))
+                   1 if clean_causal else 0, int(bwd_chunk), 0 if rank is None else 1,
+                   0 if rank is None else int(rank))
 
 
 def block_schedule(problem: Problem):
@@ -335,6 +340,12 @@ def attn_bwd_noalloc(problem, inputs: dict, work_dev, info, o_clean, o_corr, lse
     _check("csbp_attn_bwd_noalloc", st)
 
 
+def attn_bwd_noalloc_status(stream=None):
+    """csbp_attn_bwd_noalloc_status: synchronise the stream and raise if a
+    device wait of the last allocation-free backward gave up."""
+    _check("csbp_attn_bwd_noalloc_status", lib().csbp_attn_bwd_noalloc_status(_stream_ptr(stream)))
+
+
 def lse_merge(o_parts, lse_parts, o_out, lse_out, stream=None):
     """o_parts: list of fp32 [rows, Hq, d] device tensors; lse_parts: list of
     fp32 [Hq, rows]; o_out bf16 [rows, Hq, d]; lse_out fp32 [Hq, rows]."""
@@ -376,11 +387,11 @@ class BlockDiffusionAttention:
     """
 
     def __init__(self, batch, L, M, Hq, Hkv, d, P=1, has_clean_queries=True, scale=None,
-                 device="cuda", window=0, clean_causal=False, bwd_chunk=0):
+                 device="cuda", window=0, clean_causal=False, bwd_chunk=0, rank=None):
         import torch
         self.problem = make_problem(batch, L, M, Hq, Hkv, d, P, has_clean_queries, scale,
                                     window=window, clean_causal=clean_causal,
-                                    bwd_chunk=bwd_chunk)
+                                    bwd_chunk=bwd_chunk, rank=rank)
         bo, co, words, info = block_schedule(self.problem)
         self.block_owner, self.chunk_owner, self.info = bo, co, info
         self.work_host = words

@@ -136,7 +136,7 @@ WsLayout ws_layout(const csbp_problem* p, int which) {
   const size_t rows = static_cast<size_t>(p->batch) * p->L;
   size_t off = kStatusBytes;
   if (which == 0) {
-    if (p->P > 1) {
+    if (p->P > 1 && !p->per_rank) {  // a rank's forward is one fused pass
       w.part_o = off;
       off += round256(static_cast<size_t>(p->P + 1) * 2 * rows * p->Hq * p->d * 4);
       w.part_lse = off;
@@ -320,7 +320,7 @@ extern "C" csbp_status csbp_kernel_timing_read_kind(int32_t kind, double* ms, in
   return CSBP_OK;
 }
 
-extern "C" int32_t csbp_version(void) { return 300; }  // 0.3.0: strided inputs
+extern "C" int32_t csbp_version(void) { return 400; }  // 0.4.0: per-rank query rows
 
 extern "C" const char* csbp_status_string(csbp_status s) {
   switch (s) {
@@ -392,9 +392,10 @@ extern "C" csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inp
   fp.lse = lse;
   fp.part_o = nullptr;
   fp.part_lse = nullptr;
-  fp.partial_mode = p.P > 1 ? 1 : 0;
+  const bool partial = p.P > 1 && !p.per_rank;  // virtual shards: partials + merge
+  fp.partial_mode = partial ? 1 : 0;
   fp.status = reinterpret_cast<int*>(ws + wl.status);
-  if (p.P > 1) {
+  if (partial) {
     fp.part_o = reinterpret_cast<float*>(ws + wl.part_o);
     fp.part_lse = reinterpret_cast<float*>(ws + wl.part_lse);
     const int64_t n_lse = static_cast<int64_t>(p.P + 1) * 2 * p.batch * p.Hq * p.L;
@@ -404,7 +405,7 @@ extern "C" csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inp
   const cudaError_t fe = launch_fwd(p.d, maps, fp, info->n_fwd_tasks, stream);
   timer_end(timed, stream);
   if (fe != cudaSuccess) return CSBP_ERR_CUDA;
-  if (p.P > 1) {
+  if (partial) {
     const int n_parts = p.P + 1;
     const int64_t slab_o = static_cast<int64_t>(p.L) * p.Hq * p.d;
     const int64_t slab_z = static_cast<int64_t>(p.Hq) * p.L;

@@ -168,6 +168,9 @@ csbp_status validate_problem(const csbp_problem* p) {
   if (p->has_clean_queries != 0 && p->has_clean_queries != 1) return CSBP_ERR_INVALID;
   if (p->window < 0 || (p->clean_causal != 0 && p->clean_causal != 1)) return CSBP_ERR_INVALID;
   if (p->bwd_chunk < 0) return CSBP_ERR_INVALID;
+  if (p->per_rank != 0 && p->per_rank != 1) return CSBP_ERR_INVALID;
+  if (p->per_rank ? (p->P < 2 || p->rank < 0 || p->rank >= p->P) : p->rank != 0)
+    return CSBP_ERR_INVALID;
   if (p->d != 64 && p->d != 128) return CSBP_ERR_UNSUPPORTED;
   if (p->tile_q != p->tile_kv) return CSBP_ERR_UNSUPPORTED;
   // No tensor of the problem reaches 2^39 elements (1 TiB of bf16, beyond any
@@ -191,8 +194,8 @@ csbp_status validate_problem(const csbp_problem* p) {
 // the scale do not change it): lets the attention entry points refuse a list
 // built for another problem.
 uint64_t schedule_key(const csbp_problem* p) {
-  const int32_t f[9] = {p->L, p->M, p->tile_q, p->tile_kv, p->P, p->has_clean_queries,
-                        p->window, p->clean_causal, p->bwd_chunk};
+  const int32_t f[11] = {p->L, p->M, p->tile_q, p->tile_kv, p->P, p->has_clean_queries,
+                         p->window, p->clean_causal, p->bwd_chunk, p->per_rank, p->rank};
   uint64_t h = 1469598103934665603ull;
   for (int32_t v : f) {
     for (int b = 0; b < 4; ++b) {
@@ -254,13 +257,24 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
     }
   }
 
-  // ---- forward tasks: per query tile (P == 1, fused) or per (tile, part)
+  // ---- the query tiles this list covers: all, or (per_rank) those of the
+  //      two clean chunks the rank owns, in both copies (a chunk is a whole
+  //      number of tiles and of blocks, so a tile lies in one chunk and its
+  //      corrupted blocks belong to that chunk's owner)
+  const bool per_rank = problem->per_rank != 0;
+  auto owned_tile = [&](int64_t qt) {
+    return !per_rank || co[(qt * T) / chunk_len] == problem->rank;
+  };
+
+  // ---- forward tasks: per query tile (P == 1 or per_rank, fused) or per
+  //      (tile, part)
   const int n_qs = problem->has_clean_queries ? 2 : 1;
   const int q_stream0 = problem->has_clean_queries ? 0 : 1;
   std::vector<Task> fwd;
   int64_t pairs = 0;
   for (int qs = q_stream0; qs < 2; ++qs) {
     for (int64_t qt = 0; qt < nT; ++qt) {
+      if (!owned_tile(qt)) continue;
       std::vector<Seg> segs;
       std::vector<int32_t> seg_part;
       for (int ks = 0; ks < 2; ++ks) {
@@ -277,7 +291,7 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
           push_tile(segs, seg_part, ks, (int32_t)kt, cls, part);
         }
       }
-      if (P == 1) {
+      if (P == 1 || per_rank) {
         Task t{qs, (int32_t)qt, -1, segs, 0, 0};
         for (auto& s : segs) t.cost += s.end - s.begin;
         t.canon = ((int64_t)qs * nT + qt);
@@ -317,6 +331,7 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
                   },
                   kt, L, T, qa, qb);
         for (int64_t qt = qa; qt < qb; ++qt) {
+          if (!owned_tile(qt)) continue;
           const int cls = classify(qs, qt, ks, kt);
           if (!cls) continue;
           push_tile(t.segs, dummy_part, qs, (int32_t)qt, cls, 0);

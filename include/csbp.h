@@ -93,6 +93,27 @@ typedef struct {
                            gather in fp32 workspace accumulators (then
                            bf16).  A schedule setting: results differ only
                            by fp32 summation order.                      */
+  int32_t per_rank;     /* 0: every query row of the sequence (one GPU runs
+                           all P clean shards).  1: only the query rows that
+                           CSBP rank `rank` of P > 1 ranks owns -- the clean
+                           rows of its two chunks (rank and 2P-1-rank) and
+                           the corrupted rows of the blocks inside them --
+                           as one rank of a multi-GPU job runs them after
+                           the all-gather of the clean K/V shards ([Blog]
+                           "在线 softmax 合并：为什么分两段算仍是同一个注意力",
+                           implementation schedule).  The clean K/V inputs
+                           must then hold the whole clean copy; corrupted
+                           K/V rows and query rows the rank does not own are
+                           never read.  The forward is one fused pass over
+                           the owned query tiles (no partials, no merge) and
+                           writes O and LSE of the owned rows only.  The
+                           backward writes dQ of the owned rows (other rows
+                           zero), dK/dV of the owned corrupted blocks (other
+                           corrupted rows zero), and, for every clean key,
+                           the part of its dK/dV that the owned query rows
+                           contribute: the rank's addend of the owner
+                           reduce-scatter.                               */
+  int32_t rank;         /* 0 <= rank < P when per_rank == 1, else 0       */
 } csbp_problem;
 
 /* Device input tensors, bf16 [batch][L][H][d] (H = Hq for q, Hkv for k/v).
@@ -126,7 +147,8 @@ typedef struct {
   int64_t bytes;          /* size of the work list                        */
   uint64_t problem_key;   /* opaque fingerprint of the problem fields the
                              list depends on (L, M, tiles, P, query copies,
-                             window, clean_causal, bwd_chunk); the attention
+                             window, clean_causal, bwd_chunk, per_rank,
+                             rank); the attention
                              entry points refuse, with CSBP_ERR_INVALID, an
                              info whose key does not match their problem   */
 } csbp_schedule_info;
@@ -185,7 +207,8 @@ size_t csbp_workspace_bytes(const csbp_problem* problem, int which);
  *                    of each query row (copy 0 untouched without clean queries)
  * P == 1: one fused pass per query tile over all its allowed key tiles.
  * P > 1: per-part partial attention into the workspace, then the LSE merge.
- * workspace: device, >= csbp_workspace_bytes(problem, 0).               */
+ * workspace: device, >= csbp_workspace_bytes(problem, 0); its first 256
+ * bytes (the status word) zeroed before its first use (csbp_check_status). */
 csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inputs* in,
                           const void* work_dev, const csbp_schedule_info* info,
                           void* o_clean, void* o_corr, float* lse, void* workspace,
@@ -200,7 +223,8 @@ csbp_status csbp_attn_fwd(const csbp_problem* problem, const csbp_inputs* in,
  * their own block.  do_clean / dq_clean may be NULL without clean queries.
  * Needs L % 4 == 0 (the LSE and D rows are TMA-loaded), else
  * CSBP_ERR_UNSUPPORTED.
- * workspace: device, >= csbp_workspace_bytes(problem, 1).               */
+ * workspace: device, >= csbp_workspace_bytes(problem, 1); its first 256
+ * bytes (the status word) zeroed before its first use (csbp_check_status). */
 csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inputs* in,
                           const void* work_dev, const csbp_schedule_info* info,
                           const void* o_clean, const void* o_corr, const float* lse,
@@ -224,14 +248,26 @@ csbp_status csbp_attn_bwd(const csbp_problem* problem, const csbp_inputs* in,
  * device share the array and it keeps the last call's contents: each call
  * clears the part that must start at zero, and calls that can overlap on the
  * GPU (for example on two streams without ordering) race and corrupt each
- * other's results.  A device wait that timed out is not reported for this
- * variant (csbp_check_status needs the workspace).                       */
+ * other's results.  The array's address is cached per device and CUDA
+ * context (another context of the device, made current through the driver
+ * API, looks it up again); after cudaDeviceReset the device's code is
+ * reloaded, so a process that resets a device must not call this entry
+ * point on it again.  A device wait that timed out is reported by
+ * csbp_attn_bwd_noalloc_status; each call clears the status word first, so
+ * check it after the call whose result matters.                          */
 csbp_status csbp_attn_bwd_noalloc(const csbp_problem* problem, const csbp_inputs* in,
                                   const void* work_dev, const csbp_schedule_info* info,
                                   const void* o_clean, const void* o_corr, const float* lse,
                                   const void* do_clean, const void* do_corr, void* dq_clean,
                                   void* dq_corr, void* dk_clean, void* dv_clean, void* dk_corr,
                                   void* dv_corr, void* stream);
+
+/* Status of the last csbp_attn_bwd_noalloc call(s) on the current device:
+ * synchronises `stream`, then reads and clears the status word at the start
+ * of the built-in scratch array, with the codes of csbp_check_status
+ * (CSBP_ERR_TIMEOUT if a bounded device wait gave up).  It allocates
+ * nothing.  No counterpart on the method's pages.                        */
+csbp_status csbp_attn_bwd_noalloc_status(void* stream);
 
 /* Exact log-sum-exp merge of n_parts partial attentions over disjoint key
  * sets (blog section "在线 softmax 合并"): m = max_s z_s, w_s = exp(z_s - m),
@@ -248,7 +284,10 @@ csbp_status csbp_lse_merge(int32_t n_parts, const float* const* o_parts,
                            int32_t d, void* o_out, float* lse_out, void* stream);
 
 /* Synchronise `stream`, then read and clear the device status word kept at
- * the start of `workspace` by csbp_attn_fwd / csbp_attn_bwd.  Returns
+ * the start of `workspace` by csbp_attn_fwd / csbp_attn_bwd.  The entry
+ * points only ever set that word (the first 256 bytes of a workspace), so
+ * a caller zeroes it once, before the first call with a fresh workspace
+ * (cudaMemset); from then on this function clears it after each read.  Returns
  * CSBP_ERR_TIMEOUT if a bounded device wait gave up since the last check,
  * CSBP_ERR_DEVICE if a kernel refused to run: its shared-memory window was
  * not 1024-byte aligned, or (debug build, libcsbp_debug.so) a work-list
@@ -297,7 +336,8 @@ const char* csbp_status_string(csbp_status status);
  * csbp_problem.window / clean_causal / bwd_chunk, csbp_vocab_ce (with
  * csbp_vocab_ce.h), csbp_wait_selftest and csbp_kernel_timing_read_kind.
  * 0.3.0 (300) added the token and batch strides of csbp_inputs and
- * csbp_schedule_info.problem_key. */
+ * csbp_schedule_info.problem_key.  0.4.0 (400) added csbp_problem.per_rank
+ * and rank (one CSBP rank's query rows) and csbp_attn_bwd_noalloc_status. */
 int32_t csbp_version(void);
 
 #ifdef __cplusplus

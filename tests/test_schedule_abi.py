@@ -455,3 +455,62 @@ def test_entry_points_refuse_a_small_workspace_without_launching():
                            g, g, g, g, need_f - 1, None) == -3
     assert L.csbp_attn_bwd(ctypes.byref(prob), ctypes.byref(inp), g, ctypes.byref(info),
                            *([g] * 12), need_b - 1, None) == -3
+
+
+RANK_CASES = [s for s in SWEEP + random_sweep(40, 2026) if s[3] > 1]
+
+
+@pytest.mark.parametrize("L,M,T,P,clean,W,causal", RANK_CASES)
+def test_per_rank_lists_partition_the_tile_set_by_query_owner(L, M, T, P, clean, W, causal):
+    """A CSBP rank's list (per_rank = 1) holds exactly the mask's tile pairs
+    whose query tile lies in one of the rank's two clean chunks (the oracle's
+    zigzag chunk owner; the corrupted blocks of such a tile all belong to the
+    rank too), with the same full/partial flags and key parts; the forward is
+    one fused task per owned query tile; every key tile keeps a backward
+    task; and the ranks' lists partition the single-GPU list."""
+    want = O.tile_pairs(L, M, T, T, P, clean, W, causal)
+    chunk = L // (2 * P)
+    co = O.chunk_owner(L, P)
+    bo = O.block_owner(L, M, P)
+    nT = -(-L // T)
+    union = set()
+    for r in range(P):
+        prob = csbp.make_problem(1, L, M, 2, 1, 64, P=P, has_clean_queries=clean, tile=T,
+                                 window=W, clean_causal=causal, rank=r)
+        _, _, words, info = csbp.block_schedule(prob)
+        fwd, bwd, fc, bc = expand(words, info, P)
+        owned = {qt for qt in range(nT) if co[(qt * T) // chunk] == r}
+        for qt in owned:  # the corrupted blocks of an owned tile are the rank's
+            assert set(bo[qt * T // M:min((qt + 1) * T, L) // M]) <= {r}
+        mine = {x for x in want if x[1] in owned}
+        assert all(x[5] == -1 for x in fwd)
+        assert {x[:5] for x in fwd} == {x[:5] for x in mine}
+        assert bwd == mine
+        assert info.tile_pairs == len(mine)
+        assert info.n_bwd_tasks == 2 * nT
+        assert fc == sorted(fc, reverse=True) and bc == sorted(bc, reverse=True)
+        assert not (union & mine)
+        union |= mine
+    assert union == want
+
+
+def test_per_rank_needs_shards_and_a_rank_in_range():
+    for P, rank, per_rank, ok in [(1, 0, 1, False), (2, 2, 1, False), (2, -1, 1, False),
+                                  (2, 1, 0, False), (2, 1, 1, True), (4, 0, 2, False)]:
+        prob = csbp.make_problem(1, 1024, 32, 2, 1, 64, P=P)
+        prob.per_rank, prob.rank = per_rank, rank
+        info = csbp.ScheduleInfo()
+        st = csbp.lib().csbp_block_schedule(ctypes.byref(prob), None, None, None, 0,
+                                            ctypes.byref(info))
+        assert (st == -6) == ok, (P, rank, per_rank, st)   # CSBP_ERR_CAPACITY: size query
+        if not ok:
+            assert st == -1
+    # a rank's list is refused for the whole-sequence problem, and vice versa
+    a = csbp.make_problem(1, 1024, 32, 2, 1, 64, P=2)
+    b = csbp.make_problem(1, 1024, 32, 2, 1, 64, P=2, rank=1)
+    c = csbp.make_problem(1, 1024, 32, 2, 1, 64, P=2, rank=0)
+    keys = {csbp.block_schedule(x)[3].problem_key for x in (a, b, c)}
+    assert len(keys) == 3
+    # a rank's forward needs no partials: status word only
+    assert csbp.workspace_bytes(b, 0) == 256 < csbp.workspace_bytes(a, 0)
+    assert csbp.workspace_bytes(b, 1) == csbp.workspace_bytes(a, 1)
