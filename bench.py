@@ -16,8 +16,9 @@ and the outputs/gradients copied back inside the timed region.
 With N > 1 (torchrun) every rank runs an independent replica of the
 workload on its own GPU (no collective on the data path): weak scaling.
 
-Configs: the attention workloads of inputs.WORKLOADS (default dense14b;
-sharded, long, drafter, window1k, block128 .. block1024, tiny), and the
+Configs: the attention workloads of inputs.WORKLOADS (default long, the
+L = 131,072 fine-tune layer; dense14b, sharded, drafter, window1k,
+block128 .. block1024, tiny), and the
 LM-head cross-entropy workloads of inputs.CE_WORKLOADS (lmhead14b,
 lmhead_frozen, lmhead_2k), for which one step is one csbp_vocab_ce call
 (loss, dH and dW of every row) and the metric is its TFLOP/s (2 N V Dm per
@@ -40,7 +41,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "useful TFLOP/s fwd+bwd block-diffusion attention (1 GB300) and % of BF16 peak"
-DEFAULT_CONFIG = "dense14b"
+DEFAULT_CONFIG = "long"
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -81,42 +82,36 @@ def source_hash(names):
     return h.hexdigest()
 
 
-def profile_fields(path):
-    """`- key: value` lines of a committed ncu summary."""
-    fields = {}
-    if os.path.exists(path):
-        with open(path) as f:
-            for line in f:
-                if ":" in line:
-                    k, v = line.split(":", 1)
-                    fields[k.strip().strip("`- ")] = v.strip().strip("`")
-    return fields
+TRAFFIC_RECORDS = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+def recorded_dram_bytes(kernel, workload, sources):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from
+    the committed ncu records (profiles/dram_traffic.json), or None if there
+    is no record or the kernel's sources changed since it was taken."""
+    if not os.path.exists(TRAFFIC_RECORDS):
+        return None
+    with open(TRAFFIC_RECORDS) as f:
+        records = json.load(f).get("records", [])
+    want = source_hash(sources)
+    for r in records:
+        if r.get("kernel") == kernel and r.get("workload") == workload:
+            if r.get("kernel_source_sha256") != want:
+                return None
+            return int(r["dram_bytes_per_launch"])
+    return None
 
 
 def recorded_ce_traffic(workload, kernel):
     """DRAM bytes per launch of one CE GEMM (`logits_gemm`, `dh_gemm`,
-    `dw_gemm`) from the committed ncu summary, or None if there is none or
-    the kernel changed since it was taken."""
-    fields = profile_fields(os.path.join(ROOT, "profiles", f"ce_gemm_{workload}_dram.md"))
-    if fields.get("kernel_source_sha256") != source_hash(CE_KERNEL_SOURCES):
-        return None
-    try:
-        return int(fields[f"{kernel}_dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    `dw_gemm`), while the CE kernels' sources match the record."""
+    return recorded_dram_bytes(f"ce_gemm_kernel/{kernel}", workload, CE_KERNEL_SOURCES)
 
 
 def recorded_traffic(workload):
-    """DRAM bytes (read + write) per bwd_kernel launch from the committed ncu
-    summary of this workload, or None if there is none or the kernel changed
-    since it was taken."""
-    fields = profile_fields(os.path.join(ROOT, "profiles", f"bwd_kernel_{workload}_dram.md"))
-    if fields.get("kernel_source_sha256") != bwd_kernel_source_hash():
-        return None
-    try:
-        return int(fields["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    """DRAM bytes per bwd_kernel launch of this workload, while the kernel's
+    sources match the record."""
+    return recorded_dram_bytes("bwd_kernel", workload, BWD_KERNEL_SOURCES)
 
 
 # --------------------------------------------------------------- ranks
@@ -149,6 +144,29 @@ def peaks():
     return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
 
 
+# a region shorter than this is a burst for the power controller
+SUSTAINED_REGION_S = 2.0
+
+
+def choose_bf16_peak(pk, clocks, region_s):
+    """The bf16 denominator that matches how the timed region ran: the
+    sustained (power-capped) peak only when the region lasted seconds and
+    the clock record shows the power cap acting; the burst peak otherwise
+    (including when no clock record exists).  Returns (peak, name, why)."""
+    capped = bool(clocks) and "sw_power_cap" in clocks.get("reasons", [])
+    if region_s >= SUSTAINED_REGION_S and capped:
+        return (pk["bf16_sustained"], f"bf16_tflops_sustained of {pk['source']}",
+                f"timed region {region_s:.1f} s with sw_power_cap active "
+                f"in {clocks.get('power_cap_samples', 0)} of {clocks.get('samples', 0)} samples")
+    why = (f"timed region {region_s:.2f} s" + (", sw_power_cap never active" if clocks
+                                                else ", no clock record"))
+    return pk["bf16"], f"bf16_tflops of {pk['source']} (burst)", why
+
+
+def peak_fractions(tflops, pk):
+    return {"of_burst": tflops / pk["bf16"], "of_sustained": tflops / pk["bf16_sustained"]}
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
@@ -156,6 +174,8 @@ class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
@@ -167,7 +187,7 @@ class ClockSampler:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -196,7 +216,13 @@ class ClockSampler:
         self.file.seek(0)
         rows = [ln.strip().split(",") for ln in self.file if ln.strip()]
         os.unlink(self.file.name)
-        sm, mx, reasons = [], [], set()
+        return self.summarise(rows)
+
+    @staticmethod
+    def summarise(rows):
+        """Median SM clock, max clock, sample count, the throttle reasons seen
+        and how many samples had the power cap active."""
+        sm, mx, reasons, capped = [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             r = [x.strip() for x in r]
@@ -210,10 +236,12 @@ class ClockSampler:
             for n, v in zip(names, r[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+                    capped += n == "sw_power_cap"
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "reasons": sorted(reasons), "power_cap_samples": capped,
+                "period_ms": ClockSampler.PERIOD_MS}
 
 
 # ------------------------------------------------------------ cpu oracle
@@ -427,7 +455,7 @@ def bench_ce(args, w, rank, world, local):
         kernels["row_kernel"]["gbs"] = row_bytes / (kernels["row_kernel"]["ms_per_step"] * 1e-3) / 1e9
     top = max((k for k in kernels if k.endswith("gemm")), key=lambda k: kernels[k]["ms_per_step"])
     pk = peaks()
-    peak = pk["bf16_sustained"]
+    peak, peak_name, peak_why = choose_bf16_peak(pk, clocks, total_ms * 1e-3)
     top_launch_flops = gemm_flops / n_chunks
     achieved = top_launch_flops / (kernels[top]["avg_launch_ms"] * 1e-3) / 1e12
 
@@ -494,11 +522,12 @@ def bench_ce(args, w, rank, world, local):
         "config": dict(config, l2=f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB resident "
                                   f"vs {L2_BYTES / 2**20:.0f} MiB L2); no flush"),
         "pct_of_bf16_peak": value / world / peak,
+        "pct_of_bf16_peak_by_peak": peak_fractions(value / world, pk),
         "kernels": kernels,
         "roofline": {"bound": "tensor", "kernel": f"ce_gemm_kernel ({top})",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak,
-                     "peak_source": f"bf16_tflops_sustained of {pk['source']}",
+                     "frac": achieved / peak, "frac_by_peak": peak_fractions(achieved, pk),
+                     "peak_source": peak_name, "peak_choice": peak_why,
                      "launch_ms": kernels[top]["avg_launch_ms"],
                      "launches_timed": kernels[top]["launches"],
                      "traffic": recorded_ce_traffic(w.name, top)},
@@ -632,13 +661,13 @@ def main():
         e2e = run_e2e(args, w, t, attn, out, grads, stream, dev, world, flops, in_bytes)
 
     pk = peaks()
+    peak, peak_name, peak_why = choose_bf16_peak(pk, clocks, total_ms * 1e-3)
     bwd_avg = statistics.mean(bwd_ms)
     fwd_avg = statistics.mean(fwd_ms)
     bwd_call_tflops = w.useful_bwd_flops() / (bwd_avg * 1e-3) / 1e12
     bwd_kernel_ms = bwd_k_ms / max(n_bwd_k, 1)      # main kernel alone, CUDA events
     fwd_kernel_ms = fwd_k_ms / max(n_fwd_k, 1)
     achieved = w.useful_bwd_flops() / (bwd_kernel_ms * 1e-3) / 1e12
-    peak = pk["bf16_sustained"]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -646,7 +675,8 @@ def main():
         "data": "synthetic",
         "config": dict(config, l2=f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB resident "
                                   f"vs {L2_BYTES / 2**20:.0f} MiB L2); no flush"),
-        "pct_of_bf16_peak": value / world / pk["bf16_sustained"],
+        "pct_of_bf16_peak": value / world / peak,
+        "pct_of_bf16_peak_by_peak": peak_fractions(value / world, pk),
         "fwd_ms": fwd_avg, "bwd_ms": bwd_avg,
         "fwd_tflops": w.useful_fwd_flops() / (fwd_avg * 1e-3) / 1e12,
         "bwd_tflops": bwd_call_tflops,
@@ -655,8 +685,8 @@ def main():
         "fwd_kernel_ms": fwd_kernel_ms, "bwd_kernel_ms": bwd_kernel_ms,
         "roofline": {"bound": "tensor", "kernel": f"bwd_kernel<{w.d}>",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak,
-                     "peak_source": f"bf16_tflops_sustained of {pk['source']}",
+                     "frac": achieved / peak, "frac_by_peak": peak_fractions(achieved, pk),
+                     "peak_source": peak_name, "peak_choice": peak_why,
                      "launch_ms": bwd_kernel_ms, "launches_timed": n_bwd_k,
                      "traffic": recorded_traffic(w.name)},
         "hbm_kernels": hbm,

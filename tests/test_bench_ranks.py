@@ -92,3 +92,35 @@ def test_clock_sampler_child_ends_even_without_stop(monkeypatch):
     assert c.proc.poll() is not None
     got = c.stop()    # stop after the end still reads what was sampled
     assert got["sm_mhz"] == 1.0 and got["reasons"] == []
+
+
+def test_peak_follows_the_clock_record():
+    """The bf16 denominator is the burst peak unless the timed region lasted
+    seconds with the power cap active, then the sustained one."""
+    pk = {"bf16": 1914.7, "bf16_sustained": 1693.2, "hbm": 6783.8, "source": "measured"}
+    row = "0, {sm}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, {cap}"
+    short_capped = bench.ClockSampler.summarise([row.format(sm=1800, cap="Active").split(",")] * 4)
+    assert short_capped["power_cap_samples"] == 4
+    long_free = bench.ClockSampler.summarise([row.format(sm=2070, cap="Not Active").split(",")] * 9)
+    assert long_free["reasons"] == [] and long_free["sm_mhz"] == 2070.0
+    assert bench.choose_bf16_peak(pk, long_free, 20.0)[0] == 1914.7
+    assert bench.choose_bf16_peak(pk, short_capped, 0.4)[0] == 1914.7
+    assert bench.choose_bf16_peak(pk, short_capped, 20.0)[0] == 1693.2
+    assert bench.choose_bf16_peak(pk, None, 20.0)[0] == 1914.7
+    fr = bench.peak_fractions(957.35, pk)
+    assert fr["of_burst"] == pytest.approx(0.5) and fr["of_sustained"] > 0.5
+
+
+def test_traffic_records_are_keyed_by_kernel_workload_and_source(tmp_path, monkeypatch):
+    import json
+    rec = tmp_path / "dram_traffic.json"
+    sha = bench.source_hash(bench.BWD_KERNEL_SOURCES)
+    rec.write_text(json.dumps({"records": [
+        {"kernel": "bwd_kernel", "workload": "long", "dram_bytes_per_launch": 123,
+         "kernel_source_sha256": sha},
+        {"kernel": "bwd_kernel", "workload": "dense14b", "dram_bytes_per_launch": 7,
+         "kernel_source_sha256": "0" * 64}]}))
+    monkeypatch.setattr(bench, "TRAFFIC_RECORDS", str(rec))
+    assert bench.recorded_traffic("long") == 123
+    assert bench.recorded_traffic("dense14b") is None      # kernel changed since
+    assert bench.recorded_traffic("drafter") is None       # never captured

@@ -246,7 +246,7 @@ class _HostView:
         return self.t[idx].to(torch.float32).numpy()
 
 
-def _sampled_check(w, t, out, g, rows_per_head, n_keys, seed):
+def _sampled_check(w, t, out, g, rows_per_head, n_keys, walk_keys, walk_heads, seed):
     oc, ox, lse = out
     rng = np.random.default_rng(seed)
     L = w.L
@@ -270,35 +270,69 @@ def _sampled_check(w, t, out, g, rows_per_head, n_keys, seed):
     assert o_err <= TOL_O, o_err
     assert z_err <= TOL_LSE, z_err
     assert rel_fro(np.array(dq_got), np.array(dq_want)) <= TOL_REL
-    # keys: corrupted keys (read by their own block) and late clean keys
+    # keys: corrupted keys (read by their own block), late clean keys (read
+    # by the last blocks) and clean keys whose backward task walks many query
+    # tiles (the readers of clean key j are every later query row, so its
+    # dK/dV sum over the longest walks of the kernel); each compared
+    # element-wise, per key
     keys = []
     for _ in range(n_keys):
         g_ = int(rng.integers(0, w.Hkv))
         keys.append((1, int(rng.integers(0, L)), g_))
         keys.append((0, int(rng.integers(L - 2 * w.M, L - w.M)), g_))
+    walk = set()
+    for g_ in rng.choice(w.Hkv, size=walk_heads, replace=False):
+        for pos in walk_keys:
+            j = (pos if pos >= 0 else L + pos) + int(rng.integers(0, w.M))
+            keys.append((0, j, int(g_)))
+            walk.add((0, j, int(g_)))
     kref = O.sampled_keys(fv["q_clean"], fv["k_clean"], fv["v_clean"], fv["q_corr"], fv["k_corr"],
                           fv["v_corr"], fv["do_clean"], fv["do_corr"], w.M, w.scale, keys,
                           w.window, w.clean_causal)
     got_k, want_k, got_v, want_v = [], [], [], []
     for (ks, j, gg), (dk, dv) in kref.items():
         sfx = "clean" if ks == 0 else "corr"
-        got_k.append(g["dk_" + sfx][0, j, gg].double().cpu().numpy())
-        got_v.append(g["dv_" + sfx][0, j, gg].double().cpu().numpy())
+        a_k = g["dk_" + sfx][0, j, gg].double().cpu().numpy()
+        a_v = g["dv_" + sfx][0, j, gg].double().cpu().numpy()
+        if (ks, j, gg) in walk:
+            # each walk key on its own: a dropped (query tile, key tile)
+            # contribution of a long walk shows in that key's row
+            assert rel_fro(a_k, dk) <= TOL_REL, (ks, j, gg, rel_fro(a_k, dk))
+            assert rel_fro(a_v, dv) <= TOL_REL, (ks, j, gg, rel_fro(a_v, dv))
+        got_k.append(a_k)
+        got_v.append(a_v)
         want_k.append(dk)
         want_v.append(dv)
     assert rel_fro(np.array(got_k), np.array(want_k)) <= TOL_REL
     assert rel_fro(np.array(got_v), np.array(want_v)) <= TOL_REL
 
 
-@pytest.mark.parametrize("name,rows,keys,seed", [("dense14b", 256, 8, 101), ("sharded", 16, 4, 102),
-                                                  ("long", 8, 4, 103), ("drafter", 2, 2, 104),
-                                                  ("window1k", 64, 8, 105),
-                                                  ("block1024", 32, 8, 106)])
-def test_full_size_workloads_sampled(name, rows, keys, seed):
+# name, query rows per head, random (corrupted, late clean) key pairs, clean
+# key positions whose tasks walk many query tiles (negative: from the end;
+# one key of each block that starts there), KV heads they are drawn on, seed.
+# The walk keys cost the oracle their readers' full rows (about 1.5 minutes
+# of host time each beyond the 16K sequences): the early and middle ones are
+# affordable on the 16K sequences only, where a block-0 key's task walks
+# every query tile of both copies; the longer workloads take a key 8,192
+# (sharded), 2,048 (long) or 1,024 (drafter) positions before the end,
+# walks of 512, 256 and 32 query-tile steps under the KV-head-major CTA order.
+FULL_SIZE = [
+    ("dense14b", 256, 8, (0, 4096, 8192), 2, 101),
+    ("sharded", 64, 4, (-8192,), 1, 102),
+    ("long", 64, 4, (-2048,), 1, 103),
+    ("drafter", 32, 2, (-1024,), 1, 104),
+    ("window1k", 64, 8, (0, 8192), 2, 105),
+    ("block1024", 32, 8, (0, 8192), 1, 106),
+]
+
+
+@pytest.mark.parametrize("name,rows,keys,walk,walk_heads,seed", FULL_SIZE,
+                         ids=[c[0] for c in FULL_SIZE])
+def test_full_size_workloads_sampled(name, rows, keys, walk, walk_heads, seed):
     w = WORKLOADS[name]
     t, out, g = run_gpu(w)
     _invariants(w, t, g)
-    _sampled_check(w, t, out, g, rows, keys, seed=seed)
+    _sampled_check(w, t, out, g, rows, keys, walk, walk_heads, seed=seed)
     del t, out, g
     torch.cuda.empty_cache()
 
