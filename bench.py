@@ -313,6 +313,10 @@ def hbm_kernels(w, csbp):
         # fp32 dK and dV read, bf16 written (windowed backward)
         9: ("dkv_convert", 2 * rows * w.Hkv * 6 * d),
     }
+    if w.e4m3:  # fp8 inputs: 1 byte read, 2 written per element; the average launch
+        n_qs = 2 if w.has_clean_queries else 1
+        elems = rows * d * (4 * w.Hkv + 2 * n_qs * w.Hq)
+        per_launch[10] = ("e4m3_decode", 3 * elems / (4 + 2 * n_qs))
     peak = peaks()["hbm"]
     out = {}
     for kind, (name, nbytes) in per_launch.items():
@@ -330,7 +334,8 @@ def launches_per_step(w):
     n_qs = 2 if w.has_clean_queries else 1
     fwd = 1 + ((1 + n_qs * w.batch) if w.P > 1 else 0)   # [fill] + fwd + [merges]
     bwd = n_qs + 1 + n_qs                                  # pre per stream + main + convert
-    return fwd + bwd
+    dec = (4 + 2 * n_qs) if w.e4m3 else 0                 # fp8 decodes: K, V x 2, Q and dO
+    return fwd + bwd + dec
 
 
 # ------------------------------------------------------- vocabulary loss
@@ -567,6 +572,8 @@ def main():
     config = {"workload": w.name, "batch": w.batch, "L": w.L, "M": w.M, "Hq": w.Hq,
               "Hkv": w.Hkv, "d": w.d, "P": w.P, "clean_queries": w.has_clean_queries,
               "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single"}
+    if w.e4m3:
+        config["inputs"] = "fp8 e4m3, per-tensor power-of-two scales, decoded to bf16 each step"
 
     if args.impl == "reference":
         if rank != 0:
@@ -603,15 +610,32 @@ def main():
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
 
-    t = make_inputs(w, dev)
+    codes = None
+    if w.e4m3:
+        # Q, K, V and dO kept in fp8 E4M3; every step decodes them into the
+        # bf16 buffers the attention reads
+        from block_diffusion_lm_gb300.inputs import make_inputs_e4m3
+        codes, scales = make_inputs_e4m3(w, dev)
+        t = {k: (csbp.e4m3_to_bf16(c, scales[k]) if c is not None else None)
+             for k, c in codes.items()}
+
+        def decode(src, dst):
+            for k, c in src.items():
+                if c is not None:
+                    csbp.e4m3_to_bf16(c, scales[k], out=dst[k], stream=stream)
+    else:
+        t = make_inputs(w, dev)
     attn = csbp.BlockDiffusionAttention(w.batch, w.L, w.M, w.Hq, w.Hkv, w.d, P=w.P,
                                         has_clean_queries=w.has_clean_queries, device=dev,
                                         window=w.window, clean_causal=w.clean_causal)
     out = attn.alloc_outputs()
     grads = attn.alloc_grads()
-    in_bytes = sum(v.numel() * v.element_size() for v in t.values() if v is not None)
+    src = codes if codes is not None else t
+    in_bytes = sum(v.numel() * v.element_size() for v in src.values() if v is not None)
 
     def step():
+        if codes is not None:
+            decode(codes, t)
         attn.forward(t, out=out, stream=stream)
         attn.backward(t, out, grads=grads, stream=stream)
 
@@ -634,6 +658,8 @@ def main():
     with torch.cuda.stream(stream):
         start_all.record(stream)
         for i in range(args.steps):
+            if codes is not None:
+                decode(codes, t)
             ev[i][0].record(stream)
             attn.forward(t, out=out, stream=stream)
             ev[i][1].record(stream)
@@ -658,7 +684,11 @@ def main():
     # ---------------- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, t, attn, out, grads, stream, dev, world, flops, in_bytes)
+        if codes is not None:
+            e2e = run_e2e(args, w, codes, attn, out, grads, stream, dev, world, flops, in_bytes,
+                          prep=lambda d_in: (decode(d_in, t), t)[1])
+        else:
+            e2e = run_e2e(args, w, t, attn, out, grads, stream, dev, world, flops, in_bytes)
 
     pk = peaks()
     peak, peak_name, peak_why = choose_bf16_peak(pk, clocks, total_ms * 1e-3)
@@ -702,12 +732,13 @@ def main():
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, t, attn, out, grads, stream, dev, world, flops, in_bytes):
+def run_e2e(args, w, t, attn, out, grads, stream, dev, world, flops, in_bytes, prep=None):
     """Same steps through the public API from pinned host inputs, with the
     outputs and gradients copied back, all inside the timed region.  Copies
     run on their own streams with two buffer sets, so step i+1's inputs go
     up and step i's results come down while step i computes; the region runs
-    from the first input copy to the last result copy."""
+    from the first input copy to the last result copy.  `prep` turns a step's
+    uploaded inputs into the attention's (the fp8 workload decodes them)."""
     import torch
     import torch.distributed as dist
 
@@ -748,8 +779,10 @@ def run_e2e(args, w, t, attn, out, grads, stream, dev, world, flops, in_bytes):
                 in_ready[k].record(up)
             stream.wait_event(in_ready[k])
             stream.wait_event(read[k])          # its outputs were copied down
-            attn.forward(d_in, out=o, stream=stream)
-            attn.backward(d_in, o, grads=g, stream=stream)
+            with torch.cuda.stream(stream):
+                x = prep(d_in) if prep is not None else d_in
+            attn.forward(x, out=o, stream=stream)
+            attn.backward(x, o, grads=g, stream=stream)
             done[k].record(stream)
             with torch.cuda.stream(down):
                 down.wait_event(done[k])

@@ -91,6 +91,8 @@ def lib():
         L.csbp_attn_bwd_noalloc.argtypes = [P(Problem), P(Inputs), vp, P(ScheduleInfo), vp, vp,
                                             vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.csbp_attn_bwd_noalloc.restype = ctypes.c_int
+        L.csbp_e4m3_to_bf16.argtypes = [vp, ctypes.c_float, vp, i64, vp]
+        L.csbp_e4m3_to_bf16.restype = ctypes.c_int
         L.csbp_attn_bwd_noalloc_status.argtypes = [vp]
         L.csbp_attn_bwd_noalloc_status.restype = ctypes.c_int
         L.csbp_lse_merge.argtypes = [i32, P(vp), P(vp), i64, i32, i32, vp, vp, vp]
@@ -344,6 +346,26 @@ def attn_bwd_noalloc_status(stream=None):
     """csbp_attn_bwd_noalloc_status: synchronise the stream and raise if a
     device wait of the last allocation-free backward gave up."""
     _check("csbp_attn_bwd_noalloc_status", lib().csbp_attn_bwd_noalloc_status(_stream_ptr(stream)))
+
+
+def e4m3_to_bf16(x, scale: float, out=None, stream=None):
+    """csbp_e4m3_to_bf16: decode fp8 E4M3 bytes (a torch uint8 or
+    float8_e4m3fn CUDA tensor) times `scale` into bf16 (out: bf16 tensor of
+    the same shape, allocated if None)."""
+    import torch
+    c = _Checks("csbp_e4m3_to_bf16")
+    if x is None or x.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        raise ValueError("csbp_e4m3_to_bf16: x must be a uint8 or float8_e4m3fn tensor")
+    if not x.is_contiguous():
+        raise ValueError("csbp_e4m3_to_bf16: x must be contiguous")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    c.tensor("out", out, torch.bfloat16, tuple(x.shape))
+    c.seen.append(("x", x))
+    c.done()
+    _check("csbp_e4m3_to_bf16", lib().csbp_e4m3_to_bf16(_ptr(x), float(scale), _ptr(out),
+                                                        x.numel(), _stream_ptr(stream)))
+    return out
 
 
 def lse_merge(o_parts, lse_parts, o_out, lse_out, stream=None):

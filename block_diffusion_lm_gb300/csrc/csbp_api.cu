@@ -27,6 +27,8 @@ cudaError_t launch_bwd_pre(int d, const void* o, const void* dO, float* Dsum, fl
 cudaError_t launch_dq_convert(const float* acc, void* dq, int64_t n_elems, float scale,
                               cudaStream_t stream);
 cudaError_t launch_fill(float* x, int64_t n, float v, cudaStream_t stream);
+cudaError_t launch_e4m3_to_bf16(const void* in, void* out, int64_t n, float scale,
+                                cudaStream_t stream);
 uint64_t schedule_key(const csbp_problem* p);
 
 namespace {
@@ -591,6 +593,21 @@ extern "C" csbp_status csbp_lse_merge(int32_t n_parts, const float* const* o_par
                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return CSBP_ERR_CUDA;
   return CSBP_OK;
+}
+
+extern "C" csbp_status csbp_e4m3_to_bf16(const void* in, float scale, void* out, int64_t n,
+                                         void* stream) {
+  constexpr int64_t kMaxElems = int64_t(1) << 40;
+  if (!in || !out || n < 0 || n >= kMaxElems) return CSBP_ERR_INVALID;
+  if (!(scale == scale) || scale == 0.f || scale > 3.0e38f || scale < -3.0e38f)
+    return CSBP_ERR_INVALID;  // NaN, zero or infinite
+  if (!aligned16(in) || !aligned16(out)) return CSBP_ERR_INVALID;
+  if (n == 0) return CSBP_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int tk = timer_begin(10, s);
+  const cudaError_t e = launch_e4m3_to_bf16(in, out, n, scale, s);
+  timer_end(tk, s);
+  return e == cudaSuccess ? CSBP_OK : CSBP_ERR_CUDA;
 }
 
 extern "C" csbp_status csbp_check_status(void* workspace, void* stream) {

@@ -35,10 +35,11 @@ bool bwd_windowed(const csbp_problem* p);
 
 // Kernel timing (csbp_kernel_timing): kinds 0 fwd, 1 bwd, 2 CE logits GEMM,
 // 3 CE row kernel, 4 CE dH GEMM, 5 CE dW GEMM, 6 LSE merge, 7 backward
-// preprocess, 8 dQ convert, 9 dK/dV convert (windowed backward).
+// preprocess, 8 dQ convert, 9 dK/dV convert (windowed backward), 10 fp8
+// E4M3 input decode.
 // timer_begin returns the pair index to close with timer_end, or -1 when not
 // recording.
-constexpr int kTimerKinds = 10;
+constexpr int kTimerKinds = 11;
 int timer_begin(int kind, void* stream);
 void timer_end(int i, void* stream);
 

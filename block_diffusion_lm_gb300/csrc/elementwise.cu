@@ -6,10 +6,12 @@
 //  * backward preprocessing D_i = sum_c dO_ic O_ic (fp32) fused with zeroing
 //    the fp32 dQ accumulator rows;
 //  * dQ accumulator (fp32) -> scaled bf16;
-//  * fill of the partial-LSE buffer with -inf (parts that read no key).
+//  * fill of the partial-LSE buffer with -inf (parts that read no key);
+//  * fp8 E4M3 inputs times a per-tensor scale -> bf16 (inputs kept in fp8).
 // Grids are sized as a multiple of the SM count and walk their range with a
 // grid stride; every access is 16-byte vectorised.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "csbp_internal.h"
@@ -120,6 +122,49 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* acc, __nv_
   }
 }
 
+// Two E4M3 values (low byte first) -> two fp32, through the hardware
+// conversion to f16x2, which is exact: every E4M3 value is an f16 value.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+  uint32_t h2;
+  const uint16_t v = static_cast<uint16_t>(two & 0xffffu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  __half2 h;
+  *reinterpret_cast<uint32_t*>(&h) = h2;
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// out[i] = bf16_rn(scale * e4m3(in[i])): 16 inputs per thread (one 16-byte
+// load, two 16-byte stores); the last n % 16 elements one per thread.
+__global__ void __launch_bounds__(256) e4m3_to_bf16_kernel(const uint8_t* in, __nv_bfloat16* out,
+                                                           int64_t n, float scale) {
+  const int64_t n16 = n >> 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += stride) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(in) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 a = e4m3x2_to_float2(w[k]);
+      const float2 b = e4m3x2_to_float2(w[k] >> 16);
+      o[2 * k] = bf16x2_bits(a.x * scale, a.y * scale);
+      o[2 * k + 1] = bf16x2_bits(b.x * scale, b.y * scale);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out) + 2 * i;
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  for (int64_t i = (n16 << 4) + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+       i < n; i += stride)
+    out[i] = __float2bfloat16_rn(e4m3x2_to_float2(in[i]).x * scale);
+}
+
 __global__ void __launch_bounds__(256) fill_kernel(float* x, int64_t n, float v) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
@@ -170,6 +215,14 @@ cudaError_t launch_dq_convert(const float* acc, void* dq, int64_t n_elems, float
   const int64_t n8 = n_elems / 8;
   dq_convert_kernel<<<grid_for(n8), 256, 0, stream>>>(acc, static_cast<__nv_bfloat16*>(dq), n8,
                                                       scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3_to_bf16(const void* in, void* out, int64_t n, float scale,
+                                cudaStream_t stream) {
+  const int64_t work = (n >> 4) > 0 ? (n >> 4) : 1;
+  e4m3_to_bf16_kernel<<<grid_for(work), 256, 0, stream>>>(
+      static_cast<const uint8_t*>(in), static_cast<__nv_bfloat16*>(out), n, scale);
   return cudaGetLastError();
 }
 

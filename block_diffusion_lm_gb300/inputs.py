@@ -34,6 +34,7 @@ class Workload:
     seed: int = 1234
     window: int = 0                      # keys less than `window` positions back (0: all)
     clean_causal: bool = False           # clean queries token-causal (else block-causal)
+    e4m3: bool = False                   # inputs kept in fp8 E4M3 (make_inputs_e4m3)
 
     @property
     def scale(self) -> float:
@@ -94,6 +95,8 @@ WORKLOADS = {
                         has_clean_queries=False, seed=1238),
     # sliding-window layer: the dense shapes with a 1,024-token window
     "window1k": Workload("window1k", 1, 16384, 32, 40, 8, 128, window=1024, seed=1239),
+    # the dense shapes with Q, K, V and dO kept in fp8 E4M3 (per-tensor scales)
+    "dense14b_fp8": Workload("dense14b_fp8", 1, 16384, 32, 40, 8, 128, seed=1235, e4m3=True),
     # the dense shapes at the larger block sizes of the pages' training recipes
     "block128": Workload("block128", 1, 16384, 128, 40, 8, 128, seed=1240),
     "block256": Workload("block256", 1, 16384, 256, 40, 8, 128, seed=1241),
@@ -136,6 +139,47 @@ def make_inputs(w: Workload, device="cuda", seed: int | None = None,
         out["q_clean"] = None
         out["do_clean"] = None
     return out
+
+
+E4M3_MAX = 448.0  # largest finite E4M3 magnitude
+
+
+def make_inputs_e4m3(w: Workload, device="cuda", seed: int | None = None,
+                     L: int | None = None):
+    """The workload's tensors drawn as in `make_inputs` (the same float32
+    values before rounding), kept in fp8 E4M3: each tensor x gets a
+    power-of-two scale s = 2^ceil(log2(max|x| / 448)) and is stored as the
+    E4M3 rounding (nearest even) of x / s.  Returns ({name: uint8 tensor of
+    the E4M3 codes}, {name: s}); names as in `make_inputs`, absent tensors
+    None."""
+    L = w.L if L is None else L
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed if seed is None else seed)
+    raw = {}
+    for name, h in (("q_clean", w.Hq), ("k_clean", w.Hkv), ("v_clean", w.Hkv),
+                    ("q_corr", w.Hq), ("k_corr", w.Hkv), ("v_corr", w.Hkv),
+                    ("do_clean", w.Hq), ("do_corr", w.Hq)):
+        if not w.has_clean_queries and name in ("q_clean", "do_clean"):
+            continue
+        raw[name] = torch.randn((w.batch, L, h, w.d), generator=g, device=device,
+                                dtype=torch.float32)
+    if w.k_scale_range is not None:
+        lo, hi = w.k_scale_range
+        s = lo + (hi - lo) * torch.rand((w.Hkv,), generator=g, device=device,
+                                        dtype=torch.float32)
+        raw["k_clean"] = raw["k_clean"] * s.view(1, 1, -1, 1)
+        raw["k_corr"] = raw["k_corr"] * s.view(1, 1, -1, 1)
+    codes, scales = {}, {}
+    for name, t in raw.items():
+        amax = float(t.abs().max().item())
+        sc = 2.0 ** math.ceil(math.log2(amax / E4M3_MAX)) if amax > 0 else 1.0
+        codes[name] = (t / sc).to(torch.float8_e4m3fn).view(torch.uint8)
+        scales[name] = sc
+    for name in ("q_clean", "do_clean"):
+        if name not in codes:
+            codes[name] = None
+            scales[name] = None
+    return codes, scales
 
 
 def to_f64(t):

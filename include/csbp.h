@@ -283,6 +283,19 @@ csbp_status csbp_lse_merge(int32_t n_parts, const float* const* o_parts,
                            const float* const* lse_parts, int64_t rows, int32_t Hq,
                            int32_t d, void* o_out, float* lse_out, void* stream);
 
+/* fp8 inputs.  Decodes n bytes of OCP 8-bit floating point, variant E4M3
+ * (sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is
+ * subnormal; no infinities; S.1111.111 is NaN) and writes, in bf16,
+ *   out[i] = bf16_rn(fp32(scale * value(in[i])))
+ * -- one fp32 multiply (exact when scale is a power of two) rounded to bf16,
+ * nearest even; NaN stays NaN.  For Q, K, V and dO kept in fp8 with one scale
+ * per tensor: decode them into bf16 buffers and call the attention entry
+ * points, whose arithmetic is unchanged (bf16 operands, fp32 accumulation).
+ * The method's pages fix no precision; this is the fp8-input workload.
+ *  in   device, n bytes;  out  device, n bf16 elements; both 16-byte aligned
+ *  0 <= n < 2^40; scale finite and nonzero, else CSBP_ERR_INVALID.       */
+csbp_status csbp_e4m3_to_bf16(const void* in, float scale, void* out, int64_t n, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word kept at
  * the start of `workspace` by csbp_attn_fwd / csbp_attn_bwd.  The entry
  * points only ever set that word (the first 256 bytes of a workspace), so
@@ -316,7 +329,8 @@ csbp_status csbp_kernel_timing_read(double* fwd_ms, int32_t* n_fwd, double* bwd_
  * of the attention calls: 6 the LSE merge (one per query stream and batch
  * entry), 7 the backward preprocess and 8 the dQ convert (one per query
  * stream), 9 the dK/dV converts of a windowed backward (one pair per key
- * stream).  One event pair per launch.  CSBP_ERR_INVALID for another kind. */
+ * stream); 10 csbp_e4m3_to_bf16.  One event pair per launch.
+ * CSBP_ERR_INVALID for another kind. */
 csbp_status csbp_kernel_timing_read_kind(int32_t kind, double* ms, int32_t* n);
 
 /* Self-test of the device hang guard: launches one small kernel on `stream`

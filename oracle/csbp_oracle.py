@@ -662,6 +662,46 @@ def sampled_keys(qc, kc, vc, qx, kx, vx, doc, dox, M, scale, samples, window=0,
 
 
 # --------------------------------------------------------------------------
+# fp8 inputs: OCP 8-bit floating point, variant E4M3
+# (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0
+#  holds the subnormals; no infinities; S.1111.111 is NaN)
+# --------------------------------------------------------------------------
+def e4m3_value(code: int) -> float:
+    """The real number an E4M3 byte encodes, from the format definition."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** (1 - 7)
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """float32 array -> the nearest bfloat16 values (ties to even), as
+    float64: keep the top 16 bits of the float32 pattern after adding half an
+    ulp of bf16 plus the tie-breaking bit; NaN stays NaN."""
+    x = np.asarray(x, np.float32)
+    bits = x.view(np.uint32).astype(np.uint64)
+    lsb = (bits >> 16) & 1
+    rounded = ((bits + 0x7FFF + lsb) >> 16) << 16
+    out = rounded.astype(np.uint32).view(np.float32).astype(np.float64)
+    out[np.isnan(x)] = np.nan
+    return out
+
+
+def e4m3_to_bf16(codes, scale: float) -> np.ndarray:
+    """bf16 values (as float64) of scale * value(code): the product in fp32
+    (one IEEE multiply of two fp32 numbers is the exact product rounded to
+    fp32), then rounded to bf16, nearest even."""
+    table = np.array([e4m3_value(c) for c in range(256)], np.float64)
+    v = table[np.asarray(codes, np.uint8)]
+    prod = (v.astype(np.float32) * np.float32(scale)).astype(np.float32)
+    return round_to_bf16(prod)
+
+
+# --------------------------------------------------------------------------
 # Useful (mask-allowed) work
 # ([Blog] "CSBP：BP 管损坏块，CP 管干净上下文": CP and CSBP compute the same legal
 #  pairs, Theta(L^2) in total)

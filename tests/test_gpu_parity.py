@@ -364,3 +364,53 @@ def test_lse_merge_entry_point_matches_oracle(n, rows, Hq, d):
     assert np.array_equal(finite, np.isfinite(got_z))
     assert np.abs(got_z[finite] - ref_z[finite]).max() <= 1e-5 * max(1.0, np.abs(ref_z[finite]).max())
     assert np.all(got_o[~finite] == 0)
+
+
+# ----------------------------------------------------------------- fp8 inputs
+def test_e4m3_decode_is_bit_exact_against_the_oracle():
+    """csbp_e4m3_to_bf16 on every E4M3 code (a ragged length, so the scalar
+    tail runs too) and several scales, bit for bit against the oracle's
+    decoding from the format definition (NaN where the code is NaN)."""
+    n = 256 * 37 + 5
+    codes = (torch.arange(n, dtype=torch.int64) * 7 % 256).to(torch.uint8)
+    for scale in (1.0, 2.0 ** -5, 128.0, 0.3, -1.7):
+        got = csbp.e4m3_to_bf16(codes.cuda(), scale).double().cpu().numpy()
+        want = O.e4m3_to_bf16(codes.numpy(), scale)
+        nan = np.isnan(want)
+        assert np.array_equal(nan, np.isnan(got)), scale
+        assert np.array_equal(got[~nan], want[~nan]), scale
+
+
+E4M3_CASES = [Workload("e4m3_small", 1, 512, 32, 4, 2, 128, seed=70, e4m3=True),
+              Workload("e4m3_drafter", 1, 384, 16, 2, 1, 64, has_clean_queries=False,
+                       k_scale_range=(0.5, 2.0), seed=71, e4m3=True)]
+
+
+@pytest.mark.parametrize("w", E4M3_CASES, ids=[w.name for w in E4M3_CASES])
+def test_e4m3_inputs_through_the_attention_match_the_oracle(w):
+    """Q, K, V and dO kept in fp8 E4M3 with power-of-two scales: decoded on
+    the GPU, then the same attention entry points; the oracle decodes the
+    same bytes itself, so both sides see identical bf16 values."""
+    from block_diffusion_lm_gb300.inputs import make_inputs_e4m3
+    codes, scales = make_inputs_e4m3(w, "cuda")
+    t = {k: (csbp.e4m3_to_bf16(c, scales[k]) if c is not None else None)
+         for k, c in codes.items()}
+    attn = csbp.BlockDiffusionAttention(w.batch, w.L, w.M, w.Hq, w.Hkv, w.d,
+                                        has_clean_queries=w.has_clean_queries)
+    oc, ox, lse = attn.forward(t)
+    g = attn.backward(t, (oc, ox, lse))
+    attn.check()
+    torch.cuda.synchronize()
+    f = {k: (O.e4m3_to_bf16(c[0].cpu().numpy(), scales[k]) if c is not None else None)
+         for k, c in codes.items()}
+    args = (f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"], f["k_corr"], f["v_corr"])
+    Oc, Ox, Z = O.bd_attention_fwd(*args, w.M, w.scale)
+    G = O.bd_attention_bwd(*args, f["do_clean"], f["do_corr"], w.M, w.scale)
+    assert np.abs(to_f64(ox[0]) - Ox).max() <= TOL_O
+    assert np.abs(to_f64(lse[0])[1] - Z[1]).max() <= TOL_LSE
+    names = ["dq_corr", "dk_clean", "dv_clean", "dk_corr", "dv_corr"]
+    if w.has_clean_queries:
+        assert np.abs(to_f64(oc[0]) - Oc).max() <= TOL_O
+        names.append("dq_clean")
+    for k in names:
+        assert rel_fro(to_f64(g[k][0]), G[k]) <= TOL_REL, k
