@@ -489,16 +489,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       float pr[kHalf];
       tmem_ld32x2(tmem + lane_base + colS, tmem + lane_base + colS + 32, pr, pr + 32);
       if (masked) {
-        // allowed query positions of this key row form one range [lo, hi)
+        // allowed query positions of this key row form one range [lo, hi);
+        // 32 columns that no key row of the warp may read give P^T = 0
+        // without their exponentials (the special-function unit bounds this)
         int lo, hi;
         allowed_query_range(qs, k_stream, kpos, kb, p.M, p.L, p.window, p.clean_causal, k_valid,
                             lo, hi);
         lo -= q0;
         hi -= q0;
 #pragma unroll
-        for (int c = 0; c < kHalf; ++c) {
-          const float pv = ex2_approx(fmaf(pr[c], sl2, -lse[c] * kLog2e));
-          pr[c] = (c >= lo && c < hi) ? pv : 0.f;
+        for (int q = 0; q < kHalf / 32; ++q) {
+          const int c0 = q * 32;
+          if (__all_sync(0xffffffffu, hi <= c0 || lo >= c0 + 32)) {
+#pragma unroll
+            for (int c = c0; c < c0 + 32; ++c) pr[c] = 0.f;
+          } else {
+#pragma unroll
+            for (int c = c0; c < c0 + 32; ++c) {
+              const float pv = ex2_approx(fmaf(pr[c], sl2, -lse[c] * kLog2e));
+              pr[c] = (c >= lo && c < hi) ? pv : 0.f;
+            }
+          }
         }
       } else {
 #pragma unroll
