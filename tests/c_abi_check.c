@@ -107,5 +107,25 @@ int main(void) {
   printf("ce_workspace %zu\n", csbp_ce_workspace_bytes(&ce));
   ce.vocab = 100; /* not a multiple of 64 */
   printf("ce_workspace_invalid %zu\n", csbp_ce_workspace_bytes(&ce));
+
+  /* one CSBP rank's rows: needs P > 1 and a rank below P */
+  p.per_rank = 1;
+  p.rank = 1;
+  st = csbp_block_schedule(&p, NULL, NULL, NULL, 0, &info);
+  printf("rank_size_query %d\n", (int)st);
+  p.rank = 2;
+  printf("rank_out_of_range %d\n", (int)csbp_block_schedule(&p, NULL, NULL, NULL, 0, &info));
+  p.per_rank = 0;
+  p.rank = 0;
+
+  /* fp8 decode: arguments are checked before any CUDA call; n = 0 is a no-op */
+  {
+    static unsigned char bytes[32] __attribute__((aligned(16)));
+    static unsigned short out[32] __attribute__((aligned(16)));
+    printf("e4m3_null %d\n", (int)csbp_e4m3_to_bf16(NULL, 1.0f, out, 16, NULL));
+    printf("e4m3_zero_scale %d\n", (int)csbp_e4m3_to_bf16(bytes, 0.0f, out, 16, NULL));
+    printf("e4m3_misaligned %d\n", (int)csbp_e4m3_to_bf16(bytes + 1, 1.0f, out, 16, NULL));
+    printf("e4m3_empty %d\n", (int)csbp_e4m3_to_bf16(bytes, 1.0f, out, 0, NULL));
+  }
   return 0;
 }

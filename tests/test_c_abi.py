@@ -73,6 +73,10 @@ def test_host_entry_points_agree_with_the_binding_and_the_oracle(c_output):
     ce = csbp.make_ce_problem(1000, 256, 4096, 0, True, 0.001)
     assert int(o["ce_workspace"]) == csbp.ce_workspace_bytes(ce) > 0
     assert int(o["ce_workspace_invalid"]) == 0
+    assert int(o["rank_size_query"]) == -6      # CSBP_ERR_CAPACITY: the size query of a valid list
+    assert int(o["rank_out_of_range"]) == -1
+    assert [int(o[k]) for k in ("e4m3_null", "e4m3_zero_scale", "e4m3_misaligned")] == [-1] * 3
+    assert int(o["e4m3_empty"]) == 0
 
 
 def test_schedule_builder_compiles_without_warnings():
