@@ -58,6 +58,8 @@ def parse():
                     help="skip the host-buffer end-to-end leg (auxiliary measurements)")
     ap.add_argument("--L", type=int, default=None,
                     help="override the sequence length (profiling captures of a smaller case)")
+    ap.add_argument("--bwd-chunk", type=int, default=0,
+                    help="backward query-tile window (csbp_problem.bwd_chunk; 0: none)")
     return ap.parse_args()
 
 
@@ -574,6 +576,8 @@ def main():
               "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single"}
     if w.e4m3:
         config["inputs"] = "fp8 e4m3, per-tensor power-of-two scales, decoded to bf16 each step"
+    if args.bwd_chunk:
+        config["bwd_chunk"] = args.bwd_chunk
 
     if args.impl == "reference":
         if rank != 0:
@@ -627,7 +631,8 @@ def main():
         t = make_inputs(w, dev)
     attn = csbp.BlockDiffusionAttention(w.batch, w.L, w.M, w.Hq, w.Hkv, w.d, P=w.P,
                                         has_clean_queries=w.has_clean_queries, device=dev,
-                                        window=w.window, clean_causal=w.clean_causal)
+                                        window=w.window, clean_causal=w.clean_causal,
+                                        bwd_chunk=args.bwd_chunk)
     out = attn.alloc_outputs()
     grads = attn.alloc_grads()
     src = codes if codes is not None else t
