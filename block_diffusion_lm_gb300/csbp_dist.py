@@ -138,28 +138,35 @@ class CSBPRank:
     out, with the two exchanges around the library's per-rank kernels.
 
     Local tensors are [batch, 2C, H, d] bf16 (the rank's two chunks, chunk
-    `rank` first): q/k/v and dO of both copies.  forward() returns the local
-    (o_clean, o_corr, lse [batch, 2, Hq, 2C]); backward() the local dQ of
-    both copies, the local corrupted dK/dV, and the clean dK/dV of the rows
-    this rank owns summed over all ranks.
+    `rank` first): q/k/v and dO of both copies (no clean q / dO without clean
+    queries).  forward() returns the local (o_clean or None, o_corr,
+    lse [batch, 2, Hq, 2C]); backward() the local dQ of the query copies, the
+    local corrupted dK/dV, and the clean dK/dV of the rows this rank owns
+    summed over all ranks.
     """
 
     def __init__(self, batch, L, M, Hq, Hkv, d, P, rank, group=None, device="cuda",
-                 scale=None, compute=None):
+                 scale=None, compute=None, has_clean_queries=True, window=0,
+                 clean_causal=False):
         """`compute`: the per-rank attention (forward / backward /
         alloc_outputs / alloc_grads of csbp.BlockDiffusionAttention); by
         default the library's, for this rank's query rows."""
         import torch
         self.layout = ShardLayout.build(L, M, P)
         self.rank, self.group = rank, group
+        self.has_clean = has_clean_queries
         self.attn = compute if compute is not None else csbp.BlockDiffusionAttention(
-            batch, L, M, Hq, Hkv, d, P=P, scale=scale, device=device, rank=rank)
+            batch, L, M, Hq, Hkv, d, P=P, scale=scale, device=device, rank=rank,
+            has_clean_queries=has_clean_queries, window=window, clean_causal=clean_causal)
         q_shape, kv_shape = (batch, L, Hq, d), (batch, L, Hkv, d)
         z = lambda s: torch.zeros(s, dtype=torch.bfloat16, device=device)  # noqa: E731
         # sequence-order buffers the per-rank kernels address (rows the rank
         # does not own are never read)
-        self.full = {"q_clean": z(q_shape), "q_corr": z(q_shape), "k_corr": z(kv_shape),
-                     "v_corr": z(kv_shape), "do_clean": z(q_shape), "do_corr": z(q_shape)}
+        self.full = {"q_corr": z(q_shape), "k_corr": z(kv_shape), "v_corr": z(kv_shape),
+                     "do_corr": z(q_shape)}
+        if has_clean_queries:
+            self.full["q_clean"] = z(q_shape)
+            self.full["do_clean"] = z(q_shape)
         self.out = self.attn.alloc_outputs()
         self.grads = self.attn.alloc_grads()
 
@@ -167,23 +174,25 @@ class CSBPRank:
         lay, r = self.layout, self.rank
         k_full, v_full = all_gather_clean_kv(lay, local["k_clean"], local["v_clean"], self.group)
         for n in ("q_clean", "q_corr", "k_corr", "v_corr"):
-            scatter_local_rows(lay, r, local[n], self.full[n])
-        self.inputs = {**{n: self.full[n] for n in ("q_clean", "q_corr", "k_corr", "v_corr")},
+            if n in self.full:
+                scatter_local_rows(lay, r, local[n], self.full[n])
+        self.inputs = {**{n: self.full.get(n) for n in ("q_clean", "q_corr", "k_corr", "v_corr")},
                        "k_clean": k_full, "v_clean": v_full}
         oc, ox, lse = self.attn.forward(self.inputs, out=self.out, stream=stream)
         C = lay.chunk
         lse_local = np.concatenate([np.arange(c * C, (c + 1) * C) for c in lay.chunks_of(r)])
-        return (gather_local_rows(lay, r, oc), gather_local_rows(lay, r, ox),
-                lse[..., lse_local])
+        return (gather_local_rows(lay, r, oc) if oc is not None else None,
+                gather_local_rows(lay, r, ox), lse[..., lse_local])
 
     def backward(self, local_do: dict, stream=None):
         lay, r = self.layout, self.rank
         for n in ("do_clean", "do_corr"):
-            scatter_local_rows(lay, r, local_do[n], self.full[n])
-        t = {**self.inputs, "do_clean": self.full["do_clean"], "do_corr": self.full["do_corr"]}
+            if n in self.full:
+                scatter_local_rows(lay, r, local_do[n], self.full[n])
+        t = {**self.inputs, "do_clean": self.full.get("do_clean"), "do_corr": self.full["do_corr"]}
         g = self.attn.backward(t, self.out, grads=self.grads, stream=stream)
         dk, dv = reduce_scatter_clean_grads(lay, g["dk_clean"], g["dv_clean"], self.group)
-        local = {n: gather_local_rows(lay, r, g[n]) for n in ("dq_clean", "dq_corr", "dk_corr",
-                                                              "dv_corr")}
+        local = {n: (gather_local_rows(lay, r, g[n]) if g.get(n) is not None else None)
+                 for n in ("dq_clean", "dq_corr", "dk_corr", "dv_corr")}
         local["dk_clean"], local["dv_clean"] = dk, dv
         return local

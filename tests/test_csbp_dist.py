@@ -130,8 +130,9 @@ class _OracleRankCompute:
     they contribute nothing to the clean dK/dV addend; only owned rows of
     O, LSE and dQ are read back."""
 
-    def __init__(self, L, M, Hq, Hkv, d, scale):
+    def __init__(self, L, M, Hq, Hkv, d, scale, window=0, clean_causal=False):
         self.L, self.M, self.Hq, self.Hkv, self.d, self.scale = L, M, Hq, Hkv, d, scale
+        self.window, self.clean_causal = window, clean_causal
 
     def alloc_outputs(self):
         sh = (1, self.L, self.Hq, self.d)
@@ -142,20 +143,23 @@ class _OracleRankCompute:
         return {}
 
     def forward(self, t, out=None, stream=None):
-        f = {k: v[0].double().numpy() for k, v in t.items()}
+        f = {k: (v[0].double().numpy() if v is not None else None) for k, v in t.items()}
         oc, ox, lse = O.bd_attention_fwd(f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"],
-                                         f["k_corr"], f["v_corr"], self.M, self.scale)
-        out[0][0] = torch.from_numpy(oc).to(torch.bfloat16)
+                                         f["k_corr"], f["v_corr"], self.M, self.scale,
+                                         self.window, self.clean_causal)
+        if oc is not None:
+            out[0][0] = torch.from_numpy(oc).to(torch.bfloat16)
         out[1][0] = torch.from_numpy(ox).to(torch.bfloat16)
         out[2][0] = torch.from_numpy(lse).float()
-        return out
+        return (out[0] if oc is not None else None, out[1], out[2])
 
     def backward(self, t, out, grads=None, stream=None):
-        f = {k: v[0].double().numpy() for k, v in t.items()}
+        f = {k: (v[0].double().numpy() if v is not None else None) for k, v in t.items()}
         g = O.bd_attention_bwd(f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"],
                                f["k_corr"], f["v_corr"], f["do_clean"], f["do_corr"], self.M,
-                               self.scale)
-        return {k: torch.from_numpy(g[k])[None].to(torch.bfloat16)
+                               self.scale, self.window, self.clean_causal)
+        return {k: (torch.from_numpy(g[k])[None].to(torch.bfloat16) if g.get(k) is not None
+                    else None)
                 for k in ("dq_clean", "dq_corr", "dk_clean", "dv_clean", "dk_corr", "dv_corr")}
 
 
@@ -166,40 +170,58 @@ def _inputs(L, Hq, Hkv, d, seed):
     return {k: torch.randn(1, L, h, d, generator=g).to(torch.bfloat16) for k, h in shapes.items()}
 
 
-def _e2e_case(rank, world, L, M, Hq, Hkv, d):
+def _e2e_case(rank, world, L, M, Hq, Hkv, d, clean=True, window=0, causal=False):
     scale = d ** -0.5
     full = _inputs(L, Hq, Hkv, d, seed=9)
+    if not clean:
+        full["q_clean"] = full["do_clean"] = None
     node = D.CSBPRank(1, L, M, Hq, Hkv, d, world, rank, device="cpu",
-                      compute=_OracleRankCompute(L, M, Hq, Hkv, d, scale))
+                      compute=_OracleRankCompute(L, M, Hq, Hkv, d, scale, window, causal),
+                      has_clean_queries=clean, window=window, clean_causal=causal)
     lay = node.layout
-    local = {k: D.gather_local_rows(lay, rank, v) for k, v in full.items()}
+    local = {k: (D.gather_local_rows(lay, rank, v) if v is not None else None)
+             for k, v in full.items()}
     oc, ox, lse = node.forward(local)
     grads = node.backward({"do_clean": local["do_clean"], "do_corr": local["do_corr"]})
     # the unsharded sequence, float64
-    f = {k: v[0].double().numpy() for k, v in full.items()}
+    f = {k: (v[0].double().numpy() if v is not None else None) for k, v in full.items()}
     Oc, Ox, Z = O.bd_attention_fwd(f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"],
-                                   f["k_corr"], f["v_corr"], M, scale)
+                                   f["k_corr"], f["v_corr"], M, scale, window, causal)
     G = O.bd_attention_bwd(f["q_clean"], f["k_clean"], f["v_clean"], f["q_corr"], f["k_corr"],
-                           f["v_corr"], f["do_clean"], f["do_corr"], M, scale)
+                           f["v_corr"], f["do_clean"], f["do_corr"], M, scale, window, causal)
     pos = lay.positions_of(rank)
 
     def rel(a, b):
         return float(np.linalg.norm(a - b) / np.linalg.norm(b))
 
     errs = {
-        "o_clean": np.abs(oc[0].double().numpy() - Oc[pos]).max(),
         "o_corr": np.abs(ox[0].double().numpy() - Ox[pos]).max(),
-        "lse": np.abs(lse[0].double().numpy() - Z[:, :, pos]).max(),
+        "lse": np.abs(lse[0, 1].double().numpy() - Z[1][:, pos]).max(),
     }
-    for k in ("dq_clean", "dq_corr", "dk_corr", "dv_corr", "dk_clean", "dv_clean"):
+    names = ["dq_corr", "dk_corr", "dv_corr", "dk_clean", "dv_clean"]
+    if clean:
+        errs["o_clean"] = np.abs(oc[0].double().numpy() - Oc[pos]).max()
+        errs["lse_clean"] = np.abs(lse[0, 0].double().numpy() - Z[0][:, pos]).max()
+        names.append("dq_clean")
+    else:
+        assert oc is None and grads["dq_clean"] is None
+    for k in names:
         errs[k] = rel(grads[k][0].double().numpy(), G[k][pos])
-    bad = {k: v for k, v in errs.items() if not v <= (1e-3 if k == "lse" else 1e-2)}
+    bad = {k: v for k, v in errs.items() if not v <= (1e-3 if k.startswith("lse") else 1e-2)}
     return "ok" if not bad else f"FAIL {bad}"
 
 
 @pytest.mark.parametrize("world", [2, 4])
 def test_gather_rank_attention_reduce_scatter_equals_the_unsharded_oracle(world):
     _spawn(_e2e_case, world, 1024, 16, 4, 2, 16)
+
+
+@pytest.mark.parametrize("world,clean,window,causal", [(2, False, 0, False), (4, True, 200, True)])
+def test_exchange_layer_with_corrupted_queries_only_and_a_window(world, clean, window, causal):
+    """The drafter shape (no clean queries: the clean copy is context only)
+    and a sliding window with token-causal clean queries, through the same
+    gather / per-rank attention / reduce-scatter."""
+    _spawn(_e2e_case, world, 1024, 16, 4, 2, 16, clean, window, causal)
 
 
 def test_layout_refuses_a_group_of_the_wrong_size():
