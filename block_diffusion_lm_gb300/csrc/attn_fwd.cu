@@ -313,23 +313,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       w.settle();
       int prev_in[2] = {0, 0};
       int m = 0;
-      for (; w.valid() && ok; ++m, w.next()) {
+      // Per key tile m: PV_0 of tile m-1, S_0 of tile m, PV_1 of tile m-1,
+      // S_1 of tile m.  Every S_s waits for the PV_s before it (P_s shares
+      // its columns), and that wait idles the tensor pipe; the other waits
+      // of the tile (K_m, the walk to the next tile) sit inside those two
+      // drains instead of between MMA groups.
+      for (; w.valid() && ok; ++m) {
         const int b = m & 1;
         const int pb = (m - 1) & 1;
-        if (m > 0) ok = mbar_wait(&bars[B_V_FULL + pb], ((m - 1) >> 1) & 1, p.status, abort_flag);
-        if (ok) ok = mbar_wait(&bars[B_K_FULL + b], (m >> 1) & 1, p.status, abort_flag);
-        // slot by slot: the PV of the previous tile, then the S of this one,
-        // so that one slot's softmax runs while the other slot's MMAs do
         const int in[2] = {w.in0, w.in1};
-        for (int s = 0; s < 2 && ok; ++s) {
-          if (prev_in[s]) ok = issue_pv(s, pb);
-          if (ok && in[s]) ok = issue_s(s, b);
-        }
+        if (m > 0) ok = mbar_wait(&bars[B_V_FULL + pb], ((m - 1) >> 1) & 1, p.status, abort_flag);
+        if (ok && prev_in[0]) ok = issue_pv(0, pb);
+        if (ok) ok = mbar_wait(&bars[B_K_FULL + b], (m >> 1) & 1, p.status, abort_flag);
+        if (ok && in[0]) ok = issue_s(0, b);
+        if (ok && prev_in[1]) ok = issue_pv(1, pb);
         if (!ok) break;
         if (m > 0) umma_commit(&bars[B_V_EMPTY + pb]);
+        w.next();
+        if (in[1]) ok = issue_s(1, b);
+        if (!ok) break;
         umma_commit(&bars[B_K_EMPTY + b]);
-        prev_in[0] = w.in0;
-        prev_in[1] = w.in1;
+        prev_in[0] = in[0];
+        prev_in[1] = in[1];
       }
       if (ok && m > 0) {
         const int pb = (m - 1) & 1;
