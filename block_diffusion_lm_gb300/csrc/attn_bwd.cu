@@ -204,6 +204,24 @@ __device__ __forceinline__ void allowed_query_range(int q_stream, int k_stream, 
   if (window > 0) hi = min(hi, kpos + window);
 }
 
+// P^T of two query columns: 2^(s scale log2e - LSE log2e), the two
+// exponent arguments formed in one packed instruction each step.
+__device__ __forceinline__ void p_exp2(float s0, float s1, float2 lse, uint64_t sl2x2, float& e0,
+                                       float& e1) {
+  const uint64_t nl = f2_mul(f2_pack(lse.x, lse.y), f2_pack(-kLog2e, -kLog2e));
+  float x0, x1;
+  f2_unpack(f2_fma(f2_pack(s0, s1), sl2x2, nl), x0, x1);
+  e0 = ex2_approx(x0);
+  e1 = ex2_approx(x1);
+}
+
+// dS^T = P^T o (dP^T - D) of two query columns, as a bf16 pair.
+__device__ __forceinline__ uint32_t ds_pair(float p0, float p1, float dp0, float dp1, float2 dq) {
+  float a, b;
+  f2_unpack(f2_mul(f2_pack(p0, p1), f2_sub(f2_pack(dp0, dp1), f2_pack(dq.x, dq.y))), a, b);
+  return pack_bf16x2(a, b);
+}
+
 // S^T (or dP^T) of one step: M = 128 key rows, N = 128 query rows, K = d.
 template <int D>
 __device__ __forceinline__ void issue_kq(uint32_t d_tmem, uint64_t a_kv, uint64_t b_q) {
@@ -484,6 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* lse =
           reinterpret_cast<const float*>(smem + Lay::kStat + st * Lay::kStatBytes) + hf * kHalf;
       const float* Dq = lse + kTile;
+      const float2* lse2 = reinterpret_cast<const float2*>(lse);
+      const float2* Dq2 = reinterpret_cast<const float2*>(Dq);
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const bool masked = (wk.flags & 1) || k_ragged || (q0 + kHalf > p.L);
       // ---- P^T = exp(S^T scale - LSE), written back to TMEM as bf16 pairs
       float pr[kHalf];
@@ -505,15 +526,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = c0; c < c0 + 32; ++c) pr[c] = 0.f;
           } else {
 #pragma unroll
-            for (int c = c0; c < c0 + 32; ++c) {
-              const float pv = ex2_approx(fmaf(pr[c], sl2, -lse[c] * kLog2e));
-              pr[c] = (c >= lo && c < hi) ? pv : 0.f;
+            for (int c = c0; c < c0 + 32; c += 2) {
+              float e0, e1;
+              p_exp2(pr[c], pr[c + 1], lse2[c / 2], sl2x2, e0, e1);
+              pr[c] = (c >= lo && c < hi) ? e0 : 0.f;
+              pr[c + 1] = (c + 1 >= lo && c + 1 < hi) ? e1 : 0.f;
             }
           }
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kHalf; ++c) pr[c] = ex2_approx(fmaf(pr[c], sl2, -lse[c] * kLog2e));
+        for (int c = 0; c < kHalf; c += 2) p_exp2(pr[c], pr[c + 1], lse2[c / 2], sl2x2, pr[c], pr[c + 1]);
       }
       {
         float packed[32];
@@ -549,10 +572,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float* dp = (chunk < 4) ? a + chunk * 8 : b + (chunk - 4) * 8;
           const int c0 = chunk * 8;
           uint4 v;
-          v.x = pack_bf16x2(pr[c0 + 0] * (dp[0] - Dq[c0 + 0]), pr[c0 + 1] * (dp[1] - Dq[c0 + 1]));
-          v.y = pack_bf16x2(pr[c0 + 2] * (dp[2] - Dq[c0 + 2]), pr[c0 + 3] * (dp[3] - Dq[c0 + 3]));
-          v.z = pack_bf16x2(pr[c0 + 4] * (dp[4] - Dq[c0 + 4]), pr[c0 + 5] * (dp[5] - Dq[c0 + 5]));
-          v.w = pack_bf16x2(pr[c0 + 6] * (dp[6] - Dq[c0 + 6]), pr[c0 + 7] * (dp[7] - Dq[c0 + 7]));
+          v.x = ds_pair(pr[c0 + 0], pr[c0 + 1], dp[0], dp[1], Dq2[c0 / 2 + 0]);
+          v.y = ds_pair(pr[c0 + 2], pr[c0 + 3], dp[2], dp[3], Dq2[c0 / 2 + 1]);
+          v.z = ds_pair(pr[c0 + 4], pr[c0 + 5], dp[4], dp[5], Dq2[c0 / 2 + 2]);
+          v.w = ds_pair(pr[c0 + 6], pr[c0 + 7], dp[6], dp[7], Dq2[c0 / 2 + 3]);
           *reinterpret_cast<uint4*>(xbox + sw128_offset(r, chunk)) = v;
         }
       }

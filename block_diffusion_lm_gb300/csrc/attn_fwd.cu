@@ -382,7 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                       sv + c * 32, sv + (c + 1) * 32);
         const bool ragged = (static_cast<int64_t>(w.t) + 1) * kTile > p.L;
         float mx = -INFINITY;
-        if ((w.flags & 1) || ragged || !row_valid) {
+        // bit q: no row of this warp may read a key of 32-column chunk q
+        // (warp-uniform): the max skips it, and a 64-column half with both
+        // chunks dead gets P = 0 without its exponentials
+        uint32_t dead = 0;
+        // warp-uniform: the votes below need every lane of the warp (rows
+        // past L make row_valid differ inside the last query tile)
+        if (__any_sync(0xffffffffu, (w.flags & 1) || ragged || !row_valid)) {
           // the allowed keys of this query row form one range [lo, hi)
           int lo, hi;
           allowed_key_range(q_stream, w.stream, static_cast<int>(qpos), qb, p.M, p.L, p.window,
@@ -390,13 +396,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           lo -= w.t * kTile;
           hi -= w.t * kTile;
 #pragma unroll
-          for (int c = 0; c < kTile; ++c) {
-            sv[c] = (c >= lo && c < hi) ? sv[c] : -INFINITY;
-            mx = fmaxf(mx, sv[c]);
-          }
-        } else {
+          for (int q = 0; q < kTile / 32; ++q) {
+            const int c0 = q * 32;
+            if (__all_sync(0xffffffffu, hi <= c0 || lo >= c0 + 32)) {
+              dead |= 1u << q;
 #pragma unroll
-          for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, sv[c]);
+              for (int c = c0; c < c0 + 32; ++c) sv[c] = -INFINITY;
+            } else if (!__all_sync(0xffffffffu, lo <= c0 && hi >= c0 + 32)) {
+#pragma unroll
+              for (int c = c0; c < c0 + 32; ++c) sv[c] = (c >= lo && c < hi) ? sv[c] : -INFINITY;
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kTile / 32; ++q) {
+          if (dead & (1u << q)) continue;
+#pragma unroll
+          for (int c = q * 32; c < q * 32 + 32; c += 2) mx = fmax3(mx, sv[c], sv[c + 1]);
         }
         // scores stay unscaled: the scale is positive, so the row max of the
         // scaled scores is the scaled max, and each exponent below takes the
@@ -421,20 +437,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = m_new;
         }
         const float mref_safe = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float rs = 0.f;
+        // exponent arguments and the row sum two lanes per instruction
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t negm = f2_pack(-mref_safe, -mref_safe);
+        uint64_t rs2 = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float packed[32];
+          if (((dead >> (2 * half)) & 3u) == 3u) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) packed[c] = 0.f;
+            tmem_st32(tmem + lane_base + colS + half * 32, packed);
+            continue;
+          }
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float e0 = ex2_approx(fmaf(sv[half * 64 + 2 * c], sl2, -mref_safe));
-            const float e1 = ex2_approx(fmaf(sv[half * 64 + 2 * c + 1], sl2, -mref_safe));
-            rs += e0 + e1;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(sv[half * 64 + 2 * c], sv[half * 64 + 2 * c + 1]), sl2x2, negm),
+                      x0, x1);
+            const float e0 = ex2_approx(x0);
+            const float e1 = ex2_approx(x1);
+            rs2 = f2_add(rs2, f2_pack(e0, e1));
             packed[c] = __uint_as_float(pack_bf16x2(e0, e1));
           }
           tmem_st32(tmem + lane_base + colS + half * 32, packed);
         }
-        l += rs;
+        float rs0, rs1;
+        f2_unpack(rs2, rs0, rs1);
+        l += rs0 + rs1;
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_P_FULL + s]);
