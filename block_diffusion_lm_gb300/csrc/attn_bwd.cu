@@ -39,6 +39,7 @@
 
 #include "csbp_internal.h"
 #include "device_once.h"
+#include "pair_math.cuh"
 #include "ptx_sm100.cuh"
 #include "work_checks.cuh"
 
