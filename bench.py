@@ -65,7 +65,7 @@ def parse():
 
 # Sources that determine bwd_kernel's machine code; a DRAM-traffic figure
 # counts only while their hash matches the one recorded with it.
-BWD_KERNEL_SOURCES = ("attn_bwd.cu", "ptx_sm100.cuh", "pair_math.cuh", "csbp_internal.h")
+BWD_KERNEL_SOURCES = ("attn_bwd.cu", "ptx_sm100.cuh", "pair_math.cuh", "mbar_spin.cuh", "csbp_internal.h")
 
 
 def bwd_kernel_source_hash():

@@ -39,6 +39,7 @@
 
 #include "csbp_internal.h"
 #include "device_once.h"
+#include "mbar_spin.cuh"
 #include "pair_math.cuh"
 #include "ptx_sm100.cuh"
 #include "work_checks.cuh"
@@ -395,10 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_kd = idesc_bf16_f32(128, D, false, true);   // dV, dK
     constexpr uint32_t idesc_q = idesc_bf16_f32(128, 128, true, true);   // dQ^T
     auto wait_q = [&](int i) {
-      return mbar_wait(&bars[C_Q_FULL + i % kStages], (i / kStages) & 1, p.status, abort_flag);
+      return mbar_wait_spin(&bars[C_Q_FULL + i % kStages], (i / kStages) & 1, p.status, abort_flag);
     };
     auto wait_do = [&](int i) {
-      return mbar_wait(&bars[C_DO_FULL + i % Lay::kDOStages], (i / Lay::kDOStages) & 1, p.status,
+      return mbar_wait_spin(&bars[C_DO_FULL + i % Lay::kDOStages], (i / Lay::kDOStages) & 1, p.status,
                        abort_flag);
     };
     const uint64_t k_kmaj = sdesc_sw128(sK, 16, 1024);   // K as K-major A (S^T)
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sK, (D == 64) ? static_cast<uint32_t>(Lay::kZero - Lay::kK) : Lay::kBox, 1024);
     const uint64_t x_kmaj = sdesc_sw128(sX, 16, 1024);           // dS^T as K-major A (dK)
     const uint64_t x_mn = sdesc_sw128(sX, Lay::kXBox, 1024);     // dS^T as MN-major B (dQ^T)
-    bool ok = mbar_wait(&bars[C_KV_FULL], 0, p.status, abort_flag) && wait_q(0) && wait_do(0);
+    bool ok = mbar_wait_spin(&bars[C_KV_FULL], 0, p.status, abort_flag) && wait_q(0) && wait_do(0);
     if (ok) {
       tc_fence_after_sync();
       issue_kq<D>(tmem + Lay::kColS, k_kmaj, sdesc_sw128(sQ, 16, 1024));
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t do_s = sDO + (i % Lay::kDOStages) * Lay::kTileBytes;
       const uint32_t acc0 = i > 0 ? 1u : 0u;
       // ---- dV += P^T dO, P^T in TMEM: half h's 32 packed columns at 64h
-      if (!mbar_wait(&bars[C_P_READY], i & 1, p.status, abort_flag)) break;
+      if (!mbar_wait_spin(&bars[C_P_READY], i & 1, p.status, abort_flag)) break;
       tc_fence_after_sync();
       {
         const uint64_t b = sdesc_sw128(do_s, Lay::kBox, 1024);  // dO as MN-major B
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&bars[C_DO_EMPTY + i % Lay::kDOStages]);
       // ---- dQ^T = K^T dS^T first (the compute warps wait on it), then
       //      dK += dS^T Q
-      if (!mbar_wait(&bars[C_DS_READY], i & 1, p.status, abort_flag)) break;
+      if (!mbar_wait_spin(&bars[C_DS_READY], i & 1, p.status, abort_flag)) break;
       tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk)
@@ -452,13 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&bars[C_Q_EMPTY + st]);
       if (i + 1 < n_steps) {
         // ---- S^T_{i+1}: its columns held P^T_i, consumed once dV_i is done
-        if (!mbar_wait(&bars[C_PV_DONE], i & 1, p.status, abort_flag) || !wait_q(i + 1)) break;
+        if (!mbar_wait_spin(&bars[C_PV_DONE], i & 1, p.status, abort_flag) || !wait_q(i + 1)) break;
         tc_fence_after_sync();
         issue_kq<D>(tmem + Lay::kColS, k_kmaj,
                     sdesc_sw128(sQ + ((i + 1) % kStages) * Lay::kTileBytes, 16, 1024));
         umma_commit(&bars[C_S_FULL]);
         // ---- dP^T_{i+1}: its columns held dQ^T_i, free once both halves copied it
-        if (!mbar_wait(&bars[C_DQ_FREE], i & 1, p.status, abort_flag) || !wait_do(i + 1)) break;
+        if (!mbar_wait_spin(&bars[C_DQ_FREE], i & 1, p.status, abort_flag) || !wait_do(i + 1)) break;
         tc_fence_after_sync();
         issue_kq<D>(tmem + Lay::kColDP, v_kmaj,
                     sdesc_sw128(sDO + ((i + 1) % Lay::kDOStages) * Lay::kTileBytes, 16, 1024));
