@@ -35,6 +35,7 @@
 
 #include "csbp_internal.h"
 #include "device_once.h"
+#include "mbar_spin.cuh"
 #include "pair_math.cuh"
 #include "ptx_sm100.cuh"
 #include "work_checks.cuh"
@@ -279,7 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int npv[2] = {0, 0};  // PV issued per slot
       // S_s = Q_s K^T of ring stage b into slot s's S columns
       auto issue_s = [&](int s, int b) -> bool {
-        if (npv[s] > 0 && !mbar_wait(&bars[B_PV_DONE + s], (npv[s] - 1) & 1, p.status, abort_flag))
+        if (npv[s] > 0 &&
+            !mbar_wait_spin(&bars[B_PV_DONE + s], (npv[s] - 1) & 1, p.status, abort_flag))
           return false;  // its last PV still reads the P held there
         tc_fence_after_sync();
         const uint64_t q_desc = sdesc_sw128(smem_u32(smem + Lay::kQ + s * Lay::kTileBytes), 16, 1024);

@@ -10,13 +10,16 @@
 
 #include "csbp.h"
 #include "csbp_internal.h"
+#include "mbar_spin.cuh"
 #include "ptx_sm100.cuh"
 
 namespace csbp {
 namespace {
 
-// Thread 0 waits with mbar_wait, warp 1 with the warp-collective form; both
-// on a barrier with no arrivals.  Either giving up records DEV_TIMEOUT.
+// Thread 0 waits with mbar_wait, warp 1 with the warp-collective form and
+// thread 64 with the polling form the backward's MMA issuer uses; all on a
+// barrier with no arrivals.  Any of them giving up records DEV_TIMEOUT and
+// raises the abort flag, which ends the others' waits too.
 __global__ void wait_selftest_kernel(int* status, uint64_t budget_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -28,6 +31,7 @@ __global__ void wait_selftest_kernel(int* status, uint64_t budget_ns) {
   __syncthreads();
   if (threadIdx.x == 0) mbar_wait(&bar, 0, status, &abort_flag, budget_ns);
   if ((threadIdx.x >> 5) == 1) mbar_wait_warp(&bar, 0, status, &abort_flag, budget_ns);
+  if (threadIdx.x == 64) mbar_wait_spin(&bar, 0, status, &abort_flag, budget_ns);
   __syncthreads();
 }
 
@@ -37,7 +41,7 @@ __global__ void wait_selftest_kernel(int* status, uint64_t budget_ns) {
 extern "C" csbp_status csbp_wait_selftest(int64_t budget_ns, void* workspace, void* stream) {
   if (!workspace || budget_ns < 1000 || budget_ns > 2000000000) return CSBP_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return CSBP_ERR_INVALID;
-  csbp::wait_selftest_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(
+  csbp::wait_selftest_kernel<<<1, 96, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<int*>(workspace), static_cast<uint64_t>(budget_ns));
   return cudaGetLastError() == cudaSuccess ? CSBP_OK : CSBP_ERR_CUDA;
 }
