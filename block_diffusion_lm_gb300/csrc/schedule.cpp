@@ -294,7 +294,7 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
       if (P == 1 || per_rank) {
         Task t{qs, (int32_t)qt, -1, segs, 0, 0};
         for (auto& s : segs) t.cost += s.end - s.begin;
-        t.canon = ((int64_t)qs * nT + qt);
+        t.canon = W > 0 ? (int64_t)qt * 2 + qs : ((int64_t)qs * nT + qt);
         fwd.push_back(std::move(t));
       } else {
         for (int32_t part = 0; part <= P; ++part) {
@@ -307,7 +307,7 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
           if (t.segs.empty()) continue;
           // equal-cost tasks of one part and copy sit next to each other, so
           // the two query tiles a forward CTA pairs share their key tiles
-          t.canon = ((int64_t)part * 2 + qs) * nT + qt;
+          t.canon = W > 0 ? ((int64_t)part * nT + qt) * 2 + qs : ((int64_t)part * 2 + qs) * nT + qt;
           fwd.push_back(std::move(t));
         }
       }
@@ -370,7 +370,16 @@ extern "C" csbp_status csbp_block_schedule(const csbp_problem* problem, int32_t*
     if (a.cost != b.cost) return a.cost > b.cost;
     return a.canon < b.canon;
   };
-  std::sort(fwd.begin(), fwd.end(), heavy_first);
+  // With a sliding window every query tile reads about the same number of
+  // key tiles, and the clean and the corrupted tile at one position read the
+  // same window of clean keys: forward tasks then run in (part, tile, copy)
+  // order, so a CTA's two tasks are that pair and its walk wastes one tile
+  // in twenty, where cost order would pair two corrupted (or two clean)
+  // neighbours.  Otherwise heaviest first.
+  if (W > 0)
+    std::sort(fwd.begin(), fwd.end(), [](const Task& a, const Task& b) { return a.canon < b.canon; });
+  else
+    std::sort(fwd.begin(), fwd.end(), heavy_first);
   std::sort(bwd.begin(), bwd.end(), heavy_first);
 
   int64_t n_fseg = 0, n_bseg = 0;

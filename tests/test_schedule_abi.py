@@ -52,6 +52,28 @@ def expand(words, info, P):
     return fwd, bwd, fc, bc
 
 
+def fwd_order_keys(words, info):
+    """(part, q_tile, q_stream) of every forward task, in list order."""
+    off_ft = int(words[11])
+    out = []
+    for t in range(info.n_fwd_tasks):
+        qs, qt, part = (int(x) for x in words[off_ft + 8 * t: off_ft + 8 * t + 3])
+        out.append((max(part, 0), qt, qs))
+    return out
+
+
+def assert_fwd_order(words, info, fc, W):
+    """Forward tasks are heaviest first; with a sliding window (near-equal
+    costs) they run in (part, query tile, copy) order instead, so a CTA's
+    two tasks are the clean and corrupted tiles at one position, which read
+    the same window of clean key tiles."""
+    if W == 0:
+        assert fc == sorted(fc, reverse=True)
+    else:
+        keys = fwd_order_keys(words, info)
+        assert keys == sorted(keys)
+
+
 def test_library_exports_every_declared_symbol():
     L = csbp.lib()
     names = csbp.header_functions()
@@ -123,8 +145,8 @@ def test_schedule_matches_oracle_tile_set_bit_exactly(L, M, T, P, clean, W, caus
         got_bwd = {x[:5] + ((1 if x[2] == 1 else 0),) for x in bwd}
     assert got_bwd == want
     assert info.tile_pairs == len(want)
-    # heaviest first
-    assert fc == sorted(fc, reverse=True)
+    # forward: heaviest first (by position under a window); backward: heaviest first
+    assert_fwd_order(words, info, fc, W)
     assert bc == sorted(bc, reverse=True)
     # every key tile of both copies has exactly one backward task
     nT = -(-L // T)
@@ -488,7 +510,8 @@ def test_per_rank_lists_partition_the_tile_set_by_query_owner(L, M, T, P, clean,
         assert bwd == mine
         assert info.tile_pairs == len(mine)
         assert info.n_bwd_tasks == 2 * nT
-        assert fc == sorted(fc, reverse=True) and bc == sorted(bc, reverse=True)
+        assert_fwd_order(words, info, fc, W)
+        assert bc == sorted(bc, reverse=True)
         assert not (union & mine)
         union |= mine
     assert union == want
