@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // O_s += P_s V of ring stage b, P_s (bf16 pairs) in slot s's S columns
       auto issue_pv = [&](int s, int b) -> bool {
-        if (!mbar_wait(&bars[B_P_FULL + s], npv[s] & 1, p.status, abort_flag)) return false;
+        if (!mbar_wait_spin(&bars[B_P_FULL + s], npv[s] & 1, p.status, abort_flag)) return false;
         tc_fence_after_sync();
         const uint64_t vb = sdesc_sw128(smem_u32(smem + Lay::kV + b * Lay::kTileBytes), Lay::kBoxBytes,
                                         1024);  // V, MN-major B
