@@ -15,8 +15,11 @@
 // warpgroups take its two 64-column halves in parallel.  Roles (384 threads):
 //   warp 0 lane 0  TMA producer: K, V once; per step Q (2 stages) with its LSE
 //                  and D slices
-//   warp 2 lane 0  TMA producer: dO (2 stages)
-//   warp 1 lane 0  MMA issuer, per step i:
+//   warp 2 lane 0  TMA producer: dO (one stage for d = 128, refilled while
+//                  the dK, dQ^T and S^T MMAs run; two for d = 64)
+//   warp 1 lane 0  MMA issuer (it polls its barriers, so a completed MMA
+//                  group or a compute-warp arrival is seen at once), per
+//                  step i:
 //                    dV += P_i^T dO_i        (P^T read from TMEM)
 //                    dQ_i^T = K^T dS_i^T; dK += dS_i^T Q_i   (dS^T from smem;
 //                    dQ^T first: the compute warps wait on it, not on dK)
@@ -27,9 +30,10 @@
 //                  into dS^T (bf16, into its 64-column box of a 128B-swizzled
 //                  shared tile: the K-major A operand of dK and the MN-major B
 //                  operand of dQ^T).  Then it copies its half of dQ^T
-//                  (thread t = head-dim row t) out of TMEM, stages it in its
-//                  box 32 query rows at a time and adds it into the fp32 dQ
-//                  accumulator with a TMA bulk reduce-add.
+//                  (thread t = head-dim row t) out of TMEM, stages its 64
+//                  query rows (32 in its dS^T box, 32 in a buffer of its
+//                  own) and adds them into the fp32 dQ accumulator with TMA
+//                  bulk reduce-adds.
 // TMEM columns: S^T (then P^T) at 0, dP^T (then dQ^T) at 128, dV at 256,
 // dK at 256 + d.  For d = 64 the dQ^T MMA runs with M = 128 and the upper 64
 // rows of K^T read a zero tile.  All shared state lives in the dynamic

@@ -18,7 +18,10 @@
 // threads):
 //   warp 0 lane 0  TMA producer: both Q tiles once, then K / V of each key
 //                  tile of the union into 2-stage rings
-//   warp 1 lane 0  MMA issuer, per key tile of the union and slot by slot:
+//   warp 1 lane 0  MMA issuer (it polls the two waits on its chain: a PV's
+//                  completion before the S that overwrites its P, and the
+//                  softmax's P before its PV), per key tile of the union and
+//                  slot by slot:
 //                  O_s += P_s V of the previous tile, then S_s = Q_s K^T of
 //                  this one (once that PV has read the P_s it overwrites)
 //   warps 4..7, 8..11  softmax of slot 0, 1: thread t owns query row t (TMEM
